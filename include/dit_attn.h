@@ -1,0 +1,149 @@
+/*
+ * dit_attn.h -- C ABI of libditattn.so: blockwise DiT attention with on-chip
+ * chunk merging, the standalone log-sum-exp merge and the classifier-free
+ * guidance combine, for NVIDIA B300 (sm_103a).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer is a DEVICE pointer owned by the caller.  The library
+ *    allocates no memory on any call path; it keeps one 4-byte device status
+ *    word per device in a static __device__ variable.
+ *  - Calls are asynchronous on `stream` (NULL = the legacy default stream of
+ *    the current device) and return after the launch.  A status other than
+ *    DIT_OK means nothing was launched, except DIT_ERR_LAUNCH.
+ *  - Arguments are checked on the host before anything touches the GPU:
+ *    NULL or non-16-byte-aligned pointers, non-positive or overflowing sizes
+ *    and unsupported shapes are rejected with an error code and no launch.
+ *  - Device-side waits are bounded (about one second).  A wait that runs out
+ *    makes the kernel give up without trapping and sets the status word, which
+ *    dit_last_device_status() reports as DIT_ERR_DEVICE_TIMEOUT.
+ *  - The device must be compute capability 10.3 (B300); others get
+ *    DIT_ERR_UNSUPPORTED_DEVICE.
+ *
+ * Citations name the page and the section each operation comes from; the
+ * pages print no formula, so each definition is the textbook form of what the
+ * section describes.
+ */
+#ifndef DIT_ATTN_H
+#define DIT_ATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ABI-compatible with cudaStream_t; callers may pass a cudaStream_t. */
+struct CUstream_st;
+typedef struct CUstream_st *dit_stream_t;
+
+typedef enum {
+  DIT_OK = 0,
+  DIT_ERR_INVALID_ARG = -1,        /* NULL pointer, bad size or count */
+  DIT_ERR_UNSUPPORTED_SHAPE = -2,  /* e.g. head dimension not in {64, 72, 128} */
+  DIT_ERR_MISALIGNED = -3,         /* a pointer is not 16-byte aligned */
+  DIT_ERR_UNSUPPORTED_DEVICE = -4, /* not an sm_103 device */
+  DIT_ERR_LAUNCH = -5,             /* the CUDA launch itself failed */
+  DIT_ERR_DEVICE_TIMEOUT = -6,     /* a bounded device-side wait ran out */
+  DIT_ERR_CUDA = -7                /* another CUDA runtime or driver error */
+} dit_status;
+
+/*
+ * dit_attn_fwd -- full bidirectional multi-head self-attention over a DiT token
+ * sequence, computed blockwise over n_kv_chunks contiguous K/V chunks whose
+ * partial outputs and log-sum-exps are merged on chip.
+ *
+ * Source: "xDiT: an Inference Engine for DiTs with Massive Parallelism"
+ * (abstract: attention over the token sequence, split by sequence
+ * parallelism); "SwiftFusion: Scalable Sequence Parallelism for Distributed
+ * Inference of Diffusion Transformers on GPUs" (ideas 1 and 2: ring attention
+ * and Torus attention compute one piece of K/V at a time and fold each piece's
+ * result into the output).  Per (b, h), with s_ij = q_i . k_j / sqrt(D):
+ *     LSE_i = ln sum_j exp(s_ij),   O_i = sum_j exp(s_ij - LSE_i) v_j.
+ * Chunk c covers keys [floor(c S / n), floor((c + 1) S / n)); each chunk's
+ * (O_c, LSE_c) is folded into the running result by
+ *     LSE = ln(exp(LSE) + exp(LSE_c)),
+ *     O   = exp(LSE_old - LSE) O + exp(LSE_c - LSE) O_c,
+ * so every chunk count gives the unchunked result up to rounding.
+ *
+ *   q, k, v   bf16 [B, H, S, D], contiguous, 16-byte aligned.
+ *   out       bf16 [B, H, S, D], contiguous, 16-byte aligned; must not alias
+ *             q, k or v.
+ *   lse       fp32 [B, H, S] natural-log LSE of each row, or NULL.
+ *   B, H, S   >= 1, with B * H <= 2^31 - 1 (element offsets are 64-bit).
+ *   D         64, 72 or 128 (else DIT_ERR_UNSUPPORTED_SHAPE).
+ *   n_kv_chunks  1 <= n_kv_chunks <= S (else DIT_ERR_INVALID_ARG).
+ */
+dit_status dit_attn_fwd(const void *q, const void *k, const void *v, void *out,
+                        float *lse, int B, int H, int S, int D, int n_kv_chunks,
+                        dit_stream_t stream);
+
+/*
+ * dit_attn_fwd_partials -- the per-chunk half of dit_attn_fwd: for every
+ * chunk c of the same balanced partition, writes the chunk's normalised
+ * partial output O_c and its LSE_c without merging.  This is what each device
+ * of a ring / Torus sequence-parallel split holds before the recombination
+ * ("SwiftFusion ...", ideas 1 and 2); dit_attn_merge then recombines them.
+ *
+ *   q, k, v    as for dit_attn_fwd.
+ *   partials   fp32 [n_kv_chunks, B * H * S, D], 16-byte aligned.
+ *   lses       fp32 [n_kv_chunks, B * H * S], 16-byte aligned.
+ *   Other arguments and errors as for dit_attn_fwd.
+ */
+dit_status dit_attn_fwd_partials(const void *q, const void *k, const void *v,
+                                 float *partials, float *lses, int B, int H,
+                                 int S, int D, int n_kv_chunks,
+                                 dit_stream_t stream);
+
+/*
+ * dit_attn_merge -- log-sum-exp merge of n partial attention results, the
+ * recombination step of ring / Torus sequence-parallel attention
+ * ("SwiftFusion ...", ideas 1 and 2).  For each row r:
+ *     M = max_c LSE_c[r],  LSE[r] = M + ln sum_c exp(LSE_c[r] - M),
+ *     out[r] = sum_c exp(LSE_c[r] - LSE[r]) O_c[r].
+ * A partial with LSE_c[r] = -inf has weight 0 and is not read; a row whose
+ * partials are all -inf gives out = 0, LSE = -inf.
+ *
+ *   partials  fp32 [n, rows, D], contiguous, 16-byte aligned.
+ *   lses      fp32 [n, rows], contiguous, 16-byte aligned.
+ *   n         >= 1.
+ *   out       fp32 [rows, D], 16-byte aligned; must not alias the inputs.
+ *   lse_out   fp32 [rows], or NULL.
+ *   rows      >= 1; D >= 1.
+ */
+dit_status dit_attn_merge(const float *partials, const float *lses, int n,
+                          float *out, float *lse_out, long long rows, int D,
+                          dit_stream_t stream);
+
+/*
+ * cfg_combine -- classifier-free guidance combine of the conditional and the
+ * unconditional noise predictions, out = eps_u + w (eps_c - eps_u),
+ * elementwise.  Source: "Accelerating Diffusion via Hybrid Data-Pipeline
+ * Parallelism Based on Conditional Guidance Scheduling" (Technische
+ * Zusammenfassung 2A: one path with the prompt c, one with c = empty, joined
+ * after each denoising step); "xDiT ..." (abstract: CFG parallelism).
+ *
+ *   eps_c, eps_u, out  fp32 [numel], 16-byte aligned; out may alias eps_c
+ *                      or eps_u (the operation is elementwise).
+ *   numel              >= 1.
+ */
+dit_status cfg_combine(const float *eps_c, const float *eps_u, float w,
+                       float *out, long long numel, dit_stream_t stream);
+
+/*
+ * dit_last_device_status -- synchronises `stream`, then reads and clears this
+ * device's status word.  Returns DIT_ERR_DEVICE_TIMEOUT if a kernel gave up on
+ * a bounded wait since the last call, DIT_ERR_CUDA if the synchronisation
+ * itself failed, else DIT_OK.
+ */
+dit_status dit_last_device_status(dit_stream_t stream);
+
+/* Static English text for a status code; never NULL. */
+const char *dit_status_string(dit_status status);
+
+/* Version of this ABI (incremented on any signature change). */
+int dit_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DIT_ATTN_H */

@@ -102,7 +102,13 @@ class OracleLib:
         lib.oracle_cfg_combine.argtypes = [_dptr, _dptr, ctypes.c_double, _dptr,
                                            ctypes.c_longlong]
         lib.oracle_cfg_combine.restype = ctypes.c_int
+        lib.oracle_num_threads.argtypes = []
+        lib.oracle_num_threads.restype = ctypes.c_int
         self._lib = lib
+
+    def num_threads(self) -> int:
+        """OpenMP threads the oracle's loops run on."""
+        return int(self._lib.oracle_num_threads())
 
     def attention(self, q, k, v, j0: int = 0, j1: int | None = None):
         """Attention of all queries over keys [j0, j1).  q, k, v: [..., S, D].

@@ -37,6 +37,7 @@
  * Every loop is the definition written out, with no blocking or reordering.
  */
 #include <math.h>
+#include <omp.h>
 #include <stddef.h>
 #include <stdlib.h>
 
@@ -155,4 +156,15 @@ int oracle_cfg_combine(const double *eps_c, const double *eps_u, double w,
   for (long long i = 0; i < numel; ++i)
     out[i] = eps_u[i] + w * (eps_c[i] - eps_u[i]);
   return 0;
+}
+
+/* Number of OpenMP threads the loops above run on (for reporting). */
+int oracle_num_threads(void) {
+  int n = 1;
+#pragma omp parallel
+  {
+#pragma omp single
+    n = omp_get_num_threads();
+  }
+  return n;
 }

@@ -1,0 +1,548 @@
+// attn_fwd.cuh -- blockwise DiT attention forward for sm_103a.
+//
+// What it computes ("xDiT: an Inference Engine for DiTs with Massive
+// Parallelism", abstract; "SwiftFusion: Scalable Sequence Parallelism ...",
+// ideas 1-2): for every (batch, head) and query row i,
+//     O_i = sum_j softmax_j(q_i . k_j / sqrt(D)) v_j,  LSE_i = ln sum_j exp(...)
+// with the keys split into n contiguous chunks [floor(cS/n), floor((c+1)S/n)).
+// Each chunk yields (O_c, LSE_c); they are folded into the running result by
+// log-sum-exp weights, so any chunk count reproduces unchunked attention.
+//
+// Design (one CTA = one (batch*head, pair of 128-row query tiles)):
+//   warp 0      TMA producer: Q tiles once, then K and V tiles (128 keys each)
+//               through NS-stage shared-memory rings.
+//   warp 1      allocates 512 TMEM columns; one lane issues every tcgen05.mma:
+//               S_t = Q_t K^T (SS form, fp32 in TMEM) and O_t += P_t V
+//               (TS form: P read from TMEM, V from shared memory).
+//   warps 2-5   softmax for query tile 0, warps 6-9 for query tile 1.  Each
+//               thread owns one query row (one TMEM lane): it loads its S row,
+//               takes the row max, rescales its O row in TMEM when the
+//               reference max has to move, writes P = 2^(S*scale - m) as bf16
+//               over the first 64 columns of its S row, and keeps the row sum.
+// The two softmax groups ping-pong: while one group works on its S tile the
+// tensor core runs the other tile's PV and QK^T.
+//
+// Online softmax in base 2: x = S * log2(e) / sqrt(D).  The reference max m
+// only moves when a tile's max exceeds it by more than kRescaleThreshold, so
+// P <= 2^kRescaleThreshold and O is rescaled rarely; the result is exact up to
+// rounding because O and the row sum l always share the same reference.
+//
+// Chunk merge on chip: every chunk's partial result is accumulated against
+// one shared reference max m and left unnormalised.  With
+// l_c = sum_{j in c} 2^(x_j - m) the chunk's row sum, the accumulator holds
+// A = sum_c A_c, A_c = sum_{j in c} 2^(x_j - m) v_j = l_c O_c, and each
+// finished chunk's log2-LSE, LSE_c = m + log2(l_c), is folded into the
+// running L = log2(2^L + 2^LSE_c).  The log-sum-exp merge of the normalised
+// partials, O = sum_c 2^(LSE_c - L) O_c = 2^(m - L) sum_c A_c, is therefore
+// one scale of the accumulator by 2^(m - L) at the end: no pass over O is
+// made at a chunk boundary, and the largest weight of a row stays exactly 1
+// when it sets the reference.  When m moves, the accumulator and the open
+// chunk's l_c are rescaled together; L is absolute and never rescaled.
+// Key tiles never straddle chunks: a tile that would is cut at the chunk end
+// (columns past it are masked to -inf) and the next chunk starts a new tile.
+#pragma once
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace ditk {
+
+constexpr int kBlockM = 128;           // query rows per tile = TMEM lanes
+constexpr int kBlockN = 128;           // keys per K/V tile
+constexpr int kAttnThreads = 320;      // 10 warps
+constexpr int kSwzBytes = kBlockM * 128;  // one 64-column SW128 block of 128 rows
+constexpr float kRescaleThreshold = 8.0f;
+constexpr float kLn2 = 0.693147180559945309f;
+constexpr float kLog2e = 1.442695040888963407f;
+
+// Per head-dimension layout.  The head dimension is the MMA K of QK^T and the
+// MMA N of PV.  Columns 0..63 live in a 128-byte-swizzled block; the rest in a
+// second block: 64 columns (D = 128, 128-byte swizzle) or 16 columns (D = 72,
+// 32-byte swizzle; columns 72..79 are zero-filled by TMA, so padding to 80 is
+// exact).
+template <int D>
+struct AttnCfg;
+template <>
+struct AttnCfg<64> {
+  static constexpr int kDpad = 64, kTail = 0, kStages = 4;
+};
+template <>
+struct AttnCfg<72> {
+  static constexpr int kDpad = 80, kTail = 16, kStages = 4;
+};
+template <>
+struct AttnCfg<128> {
+  static constexpr int kDpad = 128, kTail = 64, kStages = 2;
+};
+
+template <int D>
+struct AttnLayout {
+  using C = AttnCfg<D>;
+  static constexpr int kTileBytes = kSwzBytes + kBlockM * C::kTail * 2;
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = 2 * kTileBytes;
+  static constexpr int kVOff = kKOff + C::kStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + C::kStages * kTileBytes;
+  static constexpr int kNumBars = 2 + 4 * C::kStages + 7;
+  static constexpr int kTmemSlotOff = kBarOff + 8 * kNumBars;
+  static constexpr int kBytes = kTmemSlotOff + 16;
+  static constexpr int kSmemLaunch = kBytes + 1024;  // slack for 1024-byte alignment
+  static_assert(kTileBytes % 1024 == 0, "tiles must keep 1024-byte alignment");
+  static_assert(kSmemLaunch <= 232448, "shared memory budget");
+};
+
+struct AttnParams {
+  __nv_bfloat16 *out;  // merged mode: bf16 [BH, S, D]
+  float *lse;          // merged mode: fp32 [BH, S] or nullptr
+  float *partials;     // partials mode: fp32 [n, BH*S, D]
+  float *part_lse;     // partials mode: fp32 [n, BH*S]
+  long long rows_total;  // BH * S
+  int S;
+  int n_chunks;
+  int num_pairs;       // ceil(ceil(S / 128) / 2)
+  int tiles_total;     // merged mode: number of key tiles over all chunks
+  float scale_log2;    // log2(e) / sqrt(D)
+};
+
+// Walks the key tiles chunk by chunk.
+struct KvIter {
+  int S, n, c, j0, j1, t0;
+  __device__ __forceinline__ void start(int S_, int n_, int c_) {
+    S = S_;
+    n = n_;
+    c = c_;
+    j0 = static_cast<int>((static_cast<long long>(c) * S) / n);
+    j1 = static_cast<int>((static_cast<long long>(c + 1) * S) / n);
+    t0 = j0;
+  }
+  __device__ __forceinline__ int valid() const { return min(kBlockN, j1 - t0); }
+  __device__ __forceinline__ bool chunk_start() const { return t0 == j0; }
+  __device__ __forceinline__ void next() {
+    t0 += kBlockN;
+    if (t0 >= j1) {
+      ++c;
+      j0 = j1;
+      j1 = static_cast<int>((static_cast<long long>(c + 1) * S) / n);
+      t0 = j0;
+    }
+  }
+};
+
+__device__ __forceinline__ float logaddexp2(float a, float b) {
+  const float mx = fmaxf(a, b), mn = fminf(a, b);
+  if (mn == -INFINITY) return mx;
+  return mx + lg2_approx(1.0f + ex2_approx(mn - mx));
+}
+
+// ------------------------------------------------------------ MMA issue
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t tS, uint32_t q_smem, uint32_t k_smem) {
+  constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, kBlockN, false);
+#pragma unroll
+  for (int ks = 0; ks < 4; ++ks) {
+    const uint64_t a = smem_desc(q_smem + ks * 32, 16, 1024, kSwizzle128B);
+    const uint64_t b = smem_desc(k_smem + ks * 32, 16, 1024, kSwizzle128B);
+    umma_ss(tS, a, b, idesc, ks > 0 ? 1u : 0u);
+  }
+  if constexpr (D == 128) {
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      const uint64_t a = smem_desc(q_smem + kSwzBytes + ks * 32, 16, 1024, kSwizzle128B);
+      const uint64_t b = smem_desc(k_smem + kSwzBytes + ks * 32, 16, 1024, kSwizzle128B);
+      umma_ss(tS, a, b, idesc, 1u);
+    }
+  } else if constexpr (D == 72) {
+    const uint64_t a = smem_desc(q_smem + kSwzBytes, 16, 256, kSwizzle32B);
+    const uint64_t b = smem_desc(k_smem + kSwzBytes, 16, 256, kSwizzle32B);
+    umma_ss(tS, a, b, idesc, 1u);
+  }
+}
+
+// O (+)= P V: P is bf16 in TMEM (8 columns per 16 keys), V is MN-major in
+// shared memory (rows = keys, 128 bytes per row per 64-column block).
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_smem, bool accumulate) {
+  if constexpr (D == 72) {
+    constexpr uint32_t idesc_main = idesc_bf16_f32(kBlockM, 64, true);
+    constexpr uint32_t idesc_tail = idesc_bf16_f32(kBlockM, 16, true);
+#pragma unroll
+    for (int ks = 0; ks < kBlockN / 16; ++ks) {
+      const uint32_t acc = (accumulate || ks > 0) ? 1u : 0u;
+      const uint64_t b0 = smem_desc(v_smem + ks * 2048, kSwzBytes, 1024, kSwizzle128B);
+      umma_ts(tO, tP + ks * 8, b0, idesc_main, acc);
+      const uint64_t b1 = smem_desc(v_smem + kSwzBytes + ks * 512, 4096, 256, kSwizzle32B);
+      umma_ts(tO + 64, tP + ks * 8, b1, idesc_tail, acc);
+    }
+  } else {
+    constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, AttnCfg<D>::kDpad, true);
+#pragma unroll
+    for (int ks = 0; ks < kBlockN / 16; ++ks) {
+      const uint32_t acc = (accumulate || ks > 0) ? 1u : 0u;
+      const uint64_t b = smem_desc(v_smem + ks * 2048, kSwzBytes, 1024, kSwizzle128B);
+      umma_ts(tO, tP + ks * 8, b, idesc, acc);
+    }
+  }
+}
+
+// Multiplies this thread's O row (Dpad fp32 columns in TMEM) by f.  Not waited.
+template <int D>
+__device__ __forceinline__ void rescale_o(uint32_t tO, float f) {
+  constexpr int kFull = AttnCfg<D>::kDpad / 32;
+#pragma unroll
+  for (int cb = 0; cb < kFull; ++cb) {
+    uint32_t r[32];
+    tmem_ld32_wait(tO + cb * 32, r);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * f);
+    tmem_st32(tO + cb * 32, r);
+  }
+  if constexpr (AttnCfg<D>::kDpad % 32 == 16) {
+    uint32_t r[16];
+    tmem_ld16_wait(tO + kFull * 32, r);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * f);
+    tmem_st16(tO + kFull * 32, r);
+  }
+}
+
+// Writes `count` fp32 values times `sc` as bf16 (count % 8 == 0) to dst.
+__device__ __forceinline__ void store_bf16_row(__nv_bfloat16 *dst, const uint32_t *r, int count,
+                                               float sc) {
+  for (int j = 0; j < count; j += 8) {
+    uint4 v;
+    v.x = pack_bf16x2(__uint_as_float(r[j + 0]) * sc, __uint_as_float(r[j + 1]) * sc);
+    v.y = pack_bf16x2(__uint_as_float(r[j + 2]) * sc, __uint_as_float(r[j + 3]) * sc);
+    v.z = pack_bf16x2(__uint_as_float(r[j + 4]) * sc, __uint_as_float(r[j + 5]) * sc);
+    v.w = pack_bf16x2(__uint_as_float(r[j + 6]) * sc, __uint_as_float(r[j + 7]) * sc);
+    *reinterpret_cast<uint4 *>(dst + j) = v;
+  }
+}
+
+__device__ __forceinline__ void store_f32_row(float *dst, const uint32_t *r, int count, float sc) {
+  for (int j = 0; j < count; j += 4) {
+    float4 v = make_float4(__uint_as_float(r[j + 0]) * sc, __uint_as_float(r[j + 1]) * sc,
+                           __uint_as_float(r[j + 2]) * sc, __uint_as_float(r[j + 3]) * sc);
+    *reinterpret_cast<float4 *>(dst + j) = v;
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+// kPartials = false: all chunks, merged on chip, bf16 O + fp32 LSE.
+// kPartials = true : one chunk per CTA, fp32 O_c + LSE_c, no merge.
+template <int D, bool kPartials>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_q_tail,
+                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_k_tail,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_v_tail,
+                    const AttnParams p) {
+  using C = AttnCfg<D>;
+  using L = AttnLayout<D>;
+  constexpr int NS = C::kStages;
+  constexpr uint32_t kTileBytes = L::kTileBytes;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t base = (raw_base + 1023u) & ~1023u;
+  uint8_t *smem = smem_raw + (base - raw_base);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // Work unit.
+  int bh, pair, chunk_first, tiles;
+  if constexpr (kPartials) {
+    const int per_bh_chunk = p.num_pairs;
+    const int u = blockIdx.x;
+    pair = u % per_bh_chunk;
+    const int bc = u / per_bh_chunk;
+    chunk_first = bc % p.n_chunks;
+    bh = bc / p.n_chunks;
+    const long long j0 = (static_cast<long long>(chunk_first) * p.S) / p.n_chunks;
+    const long long j1 = (static_cast<long long>(chunk_first + 1) * p.S) / p.n_chunks;
+    tiles = static_cast<int>((j1 - j0 + kBlockN - 1) / kBlockN);
+  } else {
+    pair = blockIdx.x % p.num_pairs;
+    bh = blockIdx.x / p.num_pairs;
+    chunk_first = 0;
+    tiles = p.tiles_total;
+  }
+  const int q_row0 = pair * 2 * kBlockM;
+  const bool has1 = q_row0 + kBlockM < p.S;
+
+  // Shared-memory addresses.
+  const uint32_t sQ0 = base + L::kQOff;
+  const uint32_t sK0 = base + L::kKOff;
+  const uint32_t sV0 = base + L::kVOff;
+  const uint32_t bars = base + L::kBarOff;
+  auto q_full = [&](int t) { return bars + 8u * t; };
+  auto k_full = [&](int s) { return bars + 8u * (2 + s); };
+  auto k_empty = [&](int s) { return bars + 8u * (2 + NS + s); };
+  auto v_full = [&](int s) { return bars + 8u * (2 + 2 * NS + s); };
+  auto v_empty = [&](int s) { return bars + 8u * (2 + 3 * NS + s); };
+  auto s_full = [&](int t) { return bars + 8u * (2 + 4 * NS + t); };
+  auto p_full = [&](int t) { return bars + 8u * (4 + 4 * NS + t); };
+  auto o_full = [&](int t) { return bars + 8u * (6 + 4 * NS + t); };
+  const uint32_t mma_done = bars + 8u * (8 + 4 * NS);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kTmemSlotOff);
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full(0), 1);
+    mbar_init(q_full(1), 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(k_full(s), 1);
+      mbar_init(k_empty(s), 1);
+      mbar_init(v_full(s), 1);
+      mbar_init(v_empty(s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(s_full(t), 1);
+      mbar_init(p_full(t), kBlockM);
+      mbar_init(o_full(t), 1);
+    }
+    mbar_init(mma_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    if constexpr (C::kTail > 0) {
+      tma_prefetch_desc(&tm_q_tail);
+      tma_prefetch_desc(&tm_k_tail);
+      tma_prefetch_desc(&tm_v_tail);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_q = l2_policy_evict_first();
+      const uint64_t pol_kv = l2_policy_evict_last();
+      for (int t = 0; t < 2; ++t) {
+        if (t == 1 && !has1) break;
+        const uint32_t dst = sQ0 + t * kTileBytes;
+        mbar_arrive_expect_tx(q_full(t), kTileBytes);
+        tma_load_3d(dst, &tm_q, q_full(t), 0, q_row0 + t * kBlockM, bh, pol_q);
+        if constexpr (C::kTail > 0)
+          tma_load_3d(dst + kSwzBytes, &tm_q_tail, q_full(t), 64, q_row0 + t * kBlockM, bh, pol_q);
+      }
+      KvIter kv;
+      kv.start(p.S, p.n_chunks, chunk_first);
+      int k_last[NS], v_last[NS];  // last use issued on each stage, -1 if none
+#pragma unroll
+      for (int s = 0; s < NS; ++s) k_last[s] = v_last[s] = -1;
+      for (int it = 0; it < tiles; ++it) {
+        const int s = it % NS;
+        const int u = it / NS;
+        if (u > 0 && !mbar_wait(k_empty(s), (u - 1) & 1)) break;
+        const uint32_t kd = sK0 + s * kTileBytes;
+        mbar_arrive_expect_tx(k_full(s), kTileBytes);
+        tma_load_3d(kd, &tm_k, k_full(s), 0, kv.t0, bh, pol_kv);
+        if constexpr (C::kTail > 0) tma_load_3d(kd + kSwzBytes, &tm_k_tail, k_full(s), 64, kv.t0, bh, pol_kv);
+        k_last[s] = u;
+        if (u > 0 && !mbar_wait(v_empty(s), (u - 1) & 1)) break;
+        const uint32_t vd = sV0 + s * kTileBytes;
+        mbar_arrive_expect_tx(v_full(s), kTileBytes);
+        tma_load_3d(vd, &tm_v, v_full(s), 0, kv.t0, bh, pol_kv);
+        if constexpr (C::kTail > 0) tma_load_3d(vd + kSwzBytes, &tm_v_tail, v_full(s), 64, kv.t0, bh, pol_kv);
+        v_last[s] = u;
+        kv.next();
+      }
+      // Drain: every load issued must land before the CTA may exit.  Waiting on
+      // the parity of a stage's last use returns at once if it already landed.
+#pragma unroll
+      for (int s = 0; s < NS; ++s) {
+        if (k_last[s] >= 0) mbar_wait(k_full(s), k_last[s] & 1);
+        if (v_last[s] >= 0) mbar_wait(v_full(s), v_last[s] & 1);
+      }
+      if (has1) mbar_wait(q_full(1), 0);
+      mbar_wait(q_full(0), 0);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      const uint32_t tS0 = tmem_base, tS1 = tmem_base + 128;
+      const uint32_t tO0 = tmem_base + 256, tO1 = tmem_base + 384;
+      bool ok = mbar_wait(q_full(0), 0) && (!has1 || mbar_wait(q_full(1), 0));
+      tc_fence_after();
+      for (int it = 0; ok && it < tiles; ++it) {
+        const int s = it % NS, u = it / NS;
+        if (!(ok = mbar_wait(k_full(s), u & 1))) break;
+        tc_fence_after();
+        const uint32_t ks = sK0 + s * kTileBytes;
+        const int ps = (it + NS - 1) % NS;
+        const uint32_t vs = sV0 + ps * kTileBytes;
+        if (it > 0) {
+          if (!(ok = mbar_wait(p_full(0), (it - 1) & 1))) break;
+          if (!(ok = mbar_wait(v_full(ps), ((it - 1) / NS) & 1))) break;
+          tc_fence_after();
+          issue_pv<D>(tO0, tS0, vs, it > 1);
+        }
+        issue_qk<D>(tS0, sQ0, ks);
+        umma_commit(s_full(0));
+        if (has1) {
+          if (it > 0) {
+            if (!(ok = mbar_wait(p_full(1), (it - 1) & 1))) break;
+            tc_fence_after();
+            issue_pv<D>(tO1, tS1, vs, it > 1);
+          }
+          issue_qk<D>(tS1, sQ0 + kTileBytes, ks);
+          umma_commit(s_full(1));
+        }
+        if (it > 0) umma_commit(v_empty(ps));
+        umma_commit(k_empty(s));
+      }
+      if (ok) {
+        const int ls = (tiles - 1) % NS;
+        const uint32_t vs = sV0 + ls * kTileBytes;
+        ok = mbar_wait(p_full(0), (tiles - 1) & 1) && mbar_wait(v_full(ls), ((tiles - 1) / NS) & 1);
+        if (ok) {
+          tc_fence_after();
+          issue_pv<D>(tO0, tS0, vs, tiles > 1);
+          umma_commit(o_full(0));
+          if (has1 && mbar_wait(p_full(1), (tiles - 1) & 1)) {
+            tc_fence_after();
+            issue_pv<D>(tO1, tS1, vs, tiles > 1);
+            umma_commit(o_full(1));
+          }
+        }
+      }
+      umma_commit(mma_done);
+      mbar_wait(mma_done, 0);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- softmax
+    const int t = (warp - 2) >> 2;   // query tile handled by this warpgroup
+    const int quarter = warp & 3;    // TMEM lane quarter this warp may access
+    const int row_in_tile = quarter * 32 + lane;
+    if (t == 0 || has1) {
+      const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+      const uint32_t tS = tmem_base + t * 128 + lane_off;
+      const uint32_t tO = tmem_base + 256 + t * 128 + lane_off;
+      const float scale_log2 = p.scale_log2;
+      float m = -INFINITY;     // reference max, base-2 scaled units
+      float l = 0.0f;          // row sum of the current chunk
+      float l_run = -INFINITY; // merged log2-LSE of finished chunks
+      KvIter kv;
+      kv.start(p.S, p.n_chunks, chunk_first);
+      bool ok = true;
+      for (int it = 0; it < tiles; ++it) {
+        if (!(ok = mbar_wait_warp(s_full(t), it & 1))) break;
+        tc_fence_after();
+        uint32_t sr[128];
+        tmem_ld128_wait(tS, sr);
+        const int valid = kv.valid();
+        if (valid < kBlockN) {
+#pragma unroll
+          for (int j = 0; j < kBlockN; ++j)
+            if (j >= valid) sr[j] = __float_as_uint(-INFINITY);
+        }
+        float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
+        float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
+#pragma unroll
+        for (int j = 4; j < kBlockN; j += 4) {
+          mx0 = fmaxf(mx0, __uint_as_float(sr[j + 0]));
+          mx1 = fmaxf(mx1, __uint_as_float(sr[j + 1]));
+          mx2 = fmaxf(mx2, __uint_as_float(sr[j + 2]));
+          mx3 = fmaxf(mx3, __uint_as_float(sr[j + 3]));
+        }
+        const float tmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * scale_log2;
+        float o_scale = 1.0f;
+        if (kv.chunk_start() && it > 0) {
+          // The previous chunk is complete: fold its LSE into the running one.
+          // Its partial output is already in the accumulator with the shared
+          // reference m, so the O half of the merge is applied at the end.
+          l_run = logaddexp2(l_run, m + lg2_approx(l));
+          l = 0.0f;
+        }
+        if (tmax > m + kRescaleThreshold) {
+          const float f = ex2_approx(m - tmax);
+          o_scale *= f;
+          l *= f;
+          m = tmax;
+        }
+        if (it > 0 && __any_sync(0xffffffffu, o_scale != 1.0f)) rescale_o<D>(tO, o_scale);
+        const float neg_m = -m;
+        float sum0 = 0.0f, sum1 = 0.0f;
+#pragma unroll
+        for (int qtr = 0; qtr < 4; ++qtr) {
+          uint32_t pr[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float a = ex2_approx(fmaf(__uint_as_float(sr[qtr * 32 + 2 * j]), scale_log2, neg_m));
+            const float b = ex2_approx(fmaf(__uint_as_float(sr[qtr * 32 + 2 * j + 1]), scale_log2, neg_m));
+            sum0 += a;
+            sum1 += b;
+            pr[j] = pack_bf16x2(a, b);
+          }
+          tmem_st16(tS + qtr * 16, pr);
+        }
+        l += sum0 + sum1;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(p_full(t));
+        kv.next();
+      }
+      if (ok) ok = mbar_wait_warp(o_full(t), 0);
+      if (ok) {
+        tc_fence_after();
+        const float lse_c = m + lg2_approx(l);
+        const float l_new = logaddexp2(l_run, lse_c);
+        const float sc = ex2_approx(m - l_new);
+        const int row = q_row0 + t * kBlockM + row_in_tile;
+        const bool in_range = row < p.S;
+        const long long grow = static_cast<long long>(bh) * p.S + row;
+        constexpr int kFull = C::kDpad / 32;
+        if constexpr (!kPartials) {
+          __nv_bfloat16 *dst = p.out + grow * D;
+#pragma unroll
+          for (int cb = 0; cb < kFull; ++cb) {
+            uint32_t r[32];
+            tmem_ld32_wait(tO + cb * 32, r);
+            if (in_range) store_bf16_row(dst + cb * 32, r, 32, sc);
+          }
+          if constexpr (C::kDpad % 32 == 16) {
+            uint32_t r[16];
+            tmem_ld16_wait(tO + kFull * 32, r);
+            if (in_range) store_bf16_row(dst + kFull * 32, r, D - kFull * 32, sc);
+          }
+          if (in_range && p.lse != nullptr) p.lse[grow] = l_new * kLn2;
+        } else {
+          float *dst = p.partials + (static_cast<long long>(chunk_first) * p.rows_total + grow) * D;
+#pragma unroll
+          for (int cb = 0; cb < kFull; ++cb) {
+            uint32_t r[32];
+            tmem_ld32_wait(tO + cb * 32, r);
+            if (in_range) store_f32_row(dst + cb * 32, r, 32, sc);
+          }
+          if constexpr (C::kDpad % 32 == 16) {
+            uint32_t r[16];
+            tmem_ld16_wait(tO + kFull * 32, r);
+            if (in_range) store_f32_row(dst + kFull * 32, r, D - kFull * 32, sc);
+          }
+          if (in_range) p.part_lse[static_cast<long long>(chunk_first) * p.rows_total + grow] = l_new * kLn2;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+}  // namespace ditk

@@ -1,0 +1,341 @@
+// dit_attn.cu -- the C ABI of libditattn.so (declared in include/dit_attn.h):
+// argument validation, TMA descriptor encoding and kernel launches.
+//
+// Every check that can be made without the GPU is made first, so invalid
+// calls return an error code before any CUDA call.  Tensor maps are encoded
+// on the host through the driver entry point fetched by the runtime (no link
+// against libcuda).  Nothing is allocated on any call path.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "dit_attn.h"
+#include "attn_fwd.cuh"
+#include "merge_cfg.cuh"
+#include "ptx.cuh"
+
+namespace {
+
+constexpr int kAbiVersion = 1;
+constexpr int kMaxDevices = 64;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool ranges_overlap(const void *a, size_t a_bytes, const void *b, size_t b_bytes) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + b_bytes && b0 < a0 + a_bytes;
+}
+
+struct DeviceState {
+  bool probed = false;
+  bool supported = false;
+  int sm_count = 0;
+  bool attr_set[3][2] = {};  // per head-dim instantiation x partials
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Makes the stream's device current for this library's runtime and checks
+// that it is an sm_103 part.
+dit_status select_device(dit_stream_t stream, int *dev_out, DeviceState **st_out) {
+  int dev = 0;
+  cudaError_t e;
+  if (stream != nullptr) {
+    e = cudaStreamGetDevice(reinterpret_cast<cudaStream_t>(stream), &dev);
+    if (e != cudaSuccess) return DIT_ERR_CUDA;
+    e = cudaSetDevice(dev);
+    if (e != cudaSuccess) return DIT_ERR_CUDA;
+  } else {
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return DIT_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return DIT_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState &st = g_dev[dev];
+  if (!st.probed) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return DIT_ERR_CUDA;
+    st.probed = true;
+    st.supported = (major == 10 && minor == 3);
+    st.sm_count = sms;
+  }
+  if (!st.supported) return DIT_ERR_UNSUPPORTED_DEVICE;
+  *dev_out = dev;
+  *st_out = &st;
+  return DIT_OK;
+}
+
+dit_status get_encoder() {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_encode != nullptr) return DIT_OK;
+  void *fn = nullptr;
+  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return DIT_ERR_CUDA;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return DIT_OK;
+}
+
+// 3-D bf16 view [BH][S][D] of one of q, k, v; a box of `box_cols` x 128 rows.
+dit_status encode_qkv_map(CUtensorMap *map, const void *ptr, long long BH, int S, int D, int box_cols,
+                          CUtensorMapSwizzle swz) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(S) * D * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(ditk::kBlockM), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DIT_OK : DIT_ERR_CUDA;
+}
+
+int head_dim_index(int D) { return D == 64 ? 0 : (D == 72 ? 1 : (D == 128 ? 2 : -1)); }
+
+dit_status check_attn_args(const void *q, const void *k, const void *v, int B, int H, int S, int D, int n) {
+  if (q == nullptr || k == nullptr || v == nullptr) return DIT_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || S < 1 || n < 1 || n > S) return DIT_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H > 2147483647LL) return DIT_ERR_INVALID_ARG;
+  if (head_dim_index(D) < 0) return DIT_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return DIT_ERR_MISALIGNED;
+  return DIT_OK;
+}
+
+template <int D, bool kPartials>
+dit_status launch_attn(DeviceState &st, int didx, const void *q, const void *k, const void *v,
+                       const ditk::AttnParams &prm, long long BH, int S, int grid, cudaStream_t stream) {
+  using L = ditk::AttnLayout<D>;
+  auto kernel = ditk::attn_fwd_kernel<D, kPartials>;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!st.attr_set[didx][kPartials ? 1 : 0]) {
+      if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemLaunch) !=
+          cudaSuccess)
+        return DIT_ERR_CUDA;
+      st.attr_set[didx][kPartials ? 1 : 0] = true;
+    }
+  }
+  CUtensorMap mq, mq_t, mk, mk_t, mv, mv_t;
+  dit_status s;
+  if ((s = encode_qkv_map(&mq, q, BH, S, D, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != DIT_OK) return s;
+  if ((s = encode_qkv_map(&mk, k, BH, S, D, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != DIT_OK) return s;
+  if ((s = encode_qkv_map(&mv, v, BH, S, D, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != DIT_OK) return s;
+  if (D == 72) {
+    if ((s = encode_qkv_map(&mq_t, q, BH, S, D, 16, CU_TENSOR_MAP_SWIZZLE_32B)) != DIT_OK) return s;
+    if ((s = encode_qkv_map(&mk_t, k, BH, S, D, 16, CU_TENSOR_MAP_SWIZZLE_32B)) != DIT_OK) return s;
+    if ((s = encode_qkv_map(&mv_t, v, BH, S, D, 16, CU_TENSOR_MAP_SWIZZLE_32B)) != DIT_OK) return s;
+  } else {
+    mq_t = mq;
+    mk_t = mk;
+    mv_t = mv;
+  }
+  kernel<<<grid, ditk::kAttnThreads, L::kSmemLaunch, stream>>>(mq, mq_t, mk, mk_t, mv, mv_t, prm);
+  return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ERR_LAUNCH;
+}
+
+template <bool kPartials>
+dit_status attn_dispatch(const void *q, const void *k, const void *v, void *out, float *lse, float *partials,
+                         float *part_lse, int B, int H, int S, int D, int n, dit_stream_t stream) {
+  const long long BH = static_cast<long long>(B) * H;
+  const int tiles_q = (S + ditk::kBlockM - 1) / ditk::kBlockM;
+  const int num_pairs = (tiles_q + 1) / 2;
+  long long grid = BH * num_pairs * (kPartials ? n : 1);
+  if (grid > 2147483647LL) return DIT_ERR_INVALID_ARG;
+  // Key tiles over all chunks (each chunk starts a new tile).
+  long long tiles_total = 0;
+  for (int c = 0; c < n; ++c) {
+    const long long j0 = (static_cast<long long>(c) * S) / n, j1 = (static_cast<long long>(c + 1) * S) / n;
+    tiles_total += (j1 - j0 + ditk::kBlockN - 1) / ditk::kBlockN;
+  }
+  if (tiles_total > 2147483647LL) return DIT_ERR_INVALID_ARG;
+
+  int dev = 0;
+  DeviceState *st = nullptr;
+  dit_status s = select_device(stream, &dev, &st);
+  if (s != DIT_OK) return s;
+  if ((s = get_encoder()) != DIT_OK) return s;
+
+  ditk::AttnParams prm{};
+  prm.out = static_cast<__nv_bfloat16 *>(out);
+  prm.lse = lse;
+  prm.partials = partials;
+  prm.part_lse = part_lse;
+  prm.rows_total = BH * S;
+  prm.S = S;
+  prm.n_chunks = n;
+  prm.num_pairs = num_pairs;
+  prm.tiles_total = static_cast<int>(tiles_total);
+  prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  switch (D) {
+    case 64:
+      return launch_attn<64, kPartials>(*st, 0, q, k, v, prm, BH, S, static_cast<int>(grid), cs);
+    case 72:
+      return launch_attn<72, kPartials>(*st, 1, q, k, v, prm, BH, S, static_cast<int>(grid), cs);
+    default:
+      return launch_attn<128, kPartials>(*st, 2, q, k, v, prm, BH, S, static_cast<int>(grid), cs);
+  }
+}
+
+int stream_grid(const DeviceState &st, long long work_items) {
+  const long long per_wave = static_cast<long long>(st.sm_count) * 8;
+  const long long need = (work_items + ditk::kStreamThreads - 1) / ditk::kStreamThreads;
+  long long g = need < per_wave ? need : per_wave;
+  return static_cast<int>(g < 1 ? 1 : g);
+}
+
+}  // namespace
+
+extern "C" {
+
+int dit_abi_version(void) { return kAbiVersion; }
+
+const char *dit_status_string(dit_status status) {
+  switch (status) {
+    case DIT_OK:
+      return "ok";
+    case DIT_ERR_INVALID_ARG:
+      return "invalid argument (null pointer, bad size, count or aliasing)";
+    case DIT_ERR_UNSUPPORTED_SHAPE:
+      return "unsupported shape (head dimension must be 64, 72 or 128)";
+    case DIT_ERR_MISALIGNED:
+      return "pointer not 16-byte aligned";
+    case DIT_ERR_UNSUPPORTED_DEVICE:
+      return "unsupported device (needs compute capability 10.3, B300)";
+    case DIT_ERR_LAUNCH:
+      return "kernel launch failed";
+    case DIT_ERR_DEVICE_TIMEOUT:
+      return "a bounded device-side wait ran out; results are invalid";
+    case DIT_ERR_CUDA:
+      return "CUDA runtime or driver error";
+  }
+  return "unknown status";
+}
+
+dit_status dit_attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
+                        int S, int D, int n_kv_chunks, dit_stream_t stream) {
+  dit_status s = check_attn_args(q, k, v, B, H, S, D, n_kv_chunks);
+  if (s != DIT_OK) return s;
+  if (out == nullptr) return DIT_ERR_INVALID_ARG;
+  if (!aligned16(out) || (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0))
+    return DIT_ERR_MISALIGNED;
+  const size_t bytes = static_cast<size_t>(B) * H * S * D * 2;
+  if (ranges_overlap(out, bytes, q, bytes) || ranges_overlap(out, bytes, k, bytes) ||
+      ranges_overlap(out, bytes, v, bytes))
+    return DIT_ERR_INVALID_ARG;
+  if (lse != nullptr) {
+    const size_t lb = static_cast<size_t>(B) * H * S * 4;
+    if (ranges_overlap(lse, lb, q, bytes) || ranges_overlap(lse, lb, k, bytes) ||
+        ranges_overlap(lse, lb, v, bytes) || ranges_overlap(lse, lb, out, bytes))
+      return DIT_ERR_INVALID_ARG;
+  }
+  return attn_dispatch<false>(q, k, v, out, lse, nullptr, nullptr, B, H, S, D, n_kv_chunks, stream);
+}
+
+dit_status dit_attn_fwd_partials(const void *q, const void *k, const void *v, float *partials, float *lses,
+                                 int B, int H, int S, int D, int n_kv_chunks, dit_stream_t stream) {
+  dit_status s = check_attn_args(q, k, v, B, H, S, D, n_kv_chunks);
+  if (s != DIT_OK) return s;
+  if (partials == nullptr || lses == nullptr) return DIT_ERR_INVALID_ARG;
+  if (!aligned16(partials) || !aligned16(lses)) return DIT_ERR_MISALIGNED;
+  const size_t in_bytes = static_cast<size_t>(B) * H * S * D * 2;
+  const size_t p_bytes = static_cast<size_t>(n_kv_chunks) * B * H * S * D * 4;
+  const size_t l_bytes = static_cast<size_t>(n_kv_chunks) * B * H * S * 4;
+  if (ranges_overlap(partials, p_bytes, q, in_bytes) || ranges_overlap(partials, p_bytes, k, in_bytes) ||
+      ranges_overlap(partials, p_bytes, v, in_bytes) || ranges_overlap(lses, l_bytes, q, in_bytes) ||
+      ranges_overlap(lses, l_bytes, k, in_bytes) || ranges_overlap(lses, l_bytes, v, in_bytes) ||
+      ranges_overlap(lses, l_bytes, partials, p_bytes))
+    return DIT_ERR_INVALID_ARG;
+  return attn_dispatch<true>(q, k, v, nullptr, nullptr, partials, lses, B, H, S, D, n_kv_chunks, stream);
+}
+
+dit_status dit_attn_merge(const float *partials, const float *lses, int n, float *out, float *lse_out,
+                          long long rows, int D, dit_stream_t stream) {
+  if (partials == nullptr || lses == nullptr || out == nullptr) return DIT_ERR_INVALID_ARG;
+  if (n < 1 || rows < 1 || D < 1) return DIT_ERR_INVALID_ARG;
+  if (rows > (1LL << 40) / D || static_cast<long long>(n) * rows * D > (1LL << 46))
+    return DIT_ERR_INVALID_ARG;
+  if (!aligned16(partials) || !aligned16(lses) || !aligned16(out) ||
+      (lse_out != nullptr && !aligned16(lse_out)))
+    return DIT_ERR_MISALIGNED;
+  const size_t p_bytes = static_cast<size_t>(n) * rows * D * 4, l_bytes = static_cast<size_t>(n) * rows * 4;
+  const size_t o_bytes = static_cast<size_t>(rows) * D * 4, lo_bytes = static_cast<size_t>(rows) * 4;
+  if (ranges_overlap(out, o_bytes, partials, p_bytes) || ranges_overlap(out, o_bytes, lses, l_bytes))
+    return DIT_ERR_INVALID_ARG;
+  if (lse_out != nullptr &&
+      (ranges_overlap(lse_out, lo_bytes, partials, p_bytes) || ranges_overlap(lse_out, lo_bytes, lses, l_bytes) ||
+       ranges_overlap(lse_out, lo_bytes, out, o_bytes)))
+    return DIT_ERR_INVALID_ARG;
+  int dev = 0;
+  DeviceState *st = nullptr;
+  dit_status s = select_device(stream, &dev, &st);
+  if (s != DIT_OK) return s;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (D % 4 == 0) {
+    const int d4 = D / 4;
+    ditk::lse_merge_vec4_kernel<<<stream_grid(*st, rows * d4), ditk::kStreamThreads, 0, cs>>>(
+        partials, lses, n, out, lse_out, rows, d4);
+  } else {
+    ditk::lse_merge_scalar_kernel<<<stream_grid(*st, rows * D), ditk::kStreamThreads, 0, cs>>>(
+        partials, lses, n, out, lse_out, rows, D);
+  }
+  return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ERR_LAUNCH;
+}
+
+dit_status cfg_combine(const float *eps_c, const float *eps_u, float w, float *out, long long numel,
+                       dit_stream_t stream) {
+  if (eps_c == nullptr || eps_u == nullptr || out == nullptr) return DIT_ERR_INVALID_ARG;
+  if (numel < 1 || numel > (1LL << 46)) return DIT_ERR_INVALID_ARG;
+  if (!std::isfinite(w)) return DIT_ERR_INVALID_ARG;
+  if (!aligned16(eps_c) || !aligned16(eps_u) || !aligned16(out)) return DIT_ERR_MISALIGNED;
+  // out may be exactly eps_c or eps_u; any other overlap is an error.
+  const size_t bytes = static_cast<size_t>(numel) * 4;
+  if ((out != eps_c && ranges_overlap(out, bytes, eps_c, bytes)) ||
+      (out != eps_u && ranges_overlap(out, bytes, eps_u, bytes)))
+    return DIT_ERR_INVALID_ARG;
+  int dev = 0;
+  DeviceState *st = nullptr;
+  dit_status s = select_device(stream, &dev, &st);
+  if (s != DIT_OK) return s;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const long long n4 = numel / 4;
+  if (n4 > 0) {
+    ditk::cfg_combine_vec4_kernel<<<stream_grid(*st, n4), ditk::kStreamThreads, 0, cs>>>(
+        reinterpret_cast<const float4 *>(eps_c), reinterpret_cast<const float4 *>(eps_u), w,
+        reinterpret_cast<float4 *>(out), n4);
+  }
+  if (numel % 4 != 0) {
+    ditk::cfg_combine_tail_kernel<<<1, 32, 0, cs>>>(eps_c, eps_u, w, out, n4 * 4, numel);
+  }
+  return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ERR_LAUNCH;
+}
+
+dit_status dit_last_device_status(dit_stream_t stream) {
+  int dev = 0;
+  DeviceState *st = nullptr;
+  dit_status s = select_device(stream, &dev, &st);
+  if (s != DIT_OK) return s;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return DIT_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpyFromSymbol(&word, ditk::g_status, sizeof(word)) != cudaSuccess) return DIT_ERR_CUDA;
+  if (word != 0u) {
+    const unsigned int zero = 0u;
+    if (cudaMemcpyToSymbol(ditk::g_status, &zero, sizeof(zero)) != cudaSuccess) return DIT_ERR_CUDA;
+    return DIT_ERR_DEVICE_TIMEOUT;
+  }
+  return DIT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,123 @@
+// merge_cfg.cuh -- the two HBM-streaming kernels of the path.
+//
+// lse_merge: log-sum-exp merge of n partial attention results, the
+//   recombination step of ring / Torus sequence-parallel attention
+//   ("SwiftFusion: Scalable Sequence Parallelism ...", ideas 1-2):
+//     M = max_c LSE_c,  LSE = M + ln sum_c exp(LSE_c - M),
+//     out = sum_c exp(LSE_c - LSE) O_c,
+//   partials with LSE_c = -inf are skipped (weight 0, never read).
+// cfg_combine: out = eps_u + w (eps_c - eps_u), the join of the conditional
+//   and unconditional paths of classifier-free guidance ("Accelerating
+//   Diffusion via Hybrid Data-Pipeline Parallelism Based on Conditional
+//   Guidance Scheduling", Technische Zusammenfassung 2A).
+//
+// Both are pure streams: each output element is written once and each input
+// element read once, 16 bytes per thread access, consecutive threads on
+// consecutive addresses.  Grids are a multiple of the SM count with a
+// grid-stride loop.
+#pragma once
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace ditk {
+
+constexpr int kStreamThreads = 256;
+
+__device__ __forceinline__ float4 ld_stream(const float4 *p) { return __ldcs(p); }
+__device__ __forceinline__ void st_stream(float4 *p, float4 v) { __stcs(p, v); }
+
+// Row statistics: M = max, then LSE.  Returns -inf for an all -inf row.
+__device__ __forceinline__ float merged_lse(const float *__restrict__ lses, int n, long long rows,
+                                            long long r) {
+  float mx = -INFINITY;
+  for (int c = 0; c < n; ++c) mx = fmaxf(mx, __ldg(lses + c * rows + r));
+  if (mx == -INFINITY) return -INFINITY;
+  float z = 0.0f;
+  for (int c = 0; c < n; ++c) {
+    const float l = __ldg(lses + c * rows + r);
+    if (l != -INFINITY) z += __expf(l - mx);
+  }
+  return mx + __logf(z);
+}
+
+// One thread per (row, 4 columns); D % 4 == 0 and 16-byte aligned pointers.
+__global__ void __launch_bounds__(kStreamThreads)
+    lse_merge_vec4_kernel(const float *__restrict__ partials, const float *__restrict__ lses, int n,
+                          float *__restrict__ out, float *__restrict__ lse_out, long long rows, int d4) {
+  const long long total = rows * d4;
+  const long long stride = static_cast<long long>(gridDim.x) * kStreamThreads;
+  for (long long idx = static_cast<long long>(blockIdx.x) * kStreamThreads + threadIdx.x; idx < total;
+       idx += stride) {
+    const long long r = idx / d4;
+    const int c4 = static_cast<int>(idx - r * d4);
+    const float lse = merged_lse(lses, n, rows, r);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lse != -INFINITY) {
+      const float4 *src = reinterpret_cast<const float4 *>(partials) + r * d4 + c4;
+      const long long cstride = rows * d4;
+#pragma unroll 4
+      for (int c = 0; c < n; ++c) {
+        const float l = __ldg(lses + c * rows + r);
+        if (l == -INFINITY) continue;
+        const float w = __expf(l - lse);
+        const float4 v = ld_stream(src + c * cstride);
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
+      }
+    }
+    st_stream(reinterpret_cast<float4 *>(out) + idx, acc);
+    if (lse_out != nullptr && c4 == 0) lse_out[r] = lse;
+  }
+}
+
+// Fallback for D % 4 != 0: one thread per output element.
+__global__ void __launch_bounds__(kStreamThreads)
+    lse_merge_scalar_kernel(const float *__restrict__ partials, const float *__restrict__ lses, int n,
+                            float *__restrict__ out, float *__restrict__ lse_out, long long rows, int D) {
+  const long long total = rows * D;
+  const long long stride = static_cast<long long>(gridDim.x) * kStreamThreads;
+  for (long long idx = static_cast<long long>(blockIdx.x) * kStreamThreads + threadIdx.x; idx < total;
+       idx += stride) {
+    const long long r = idx / D;
+    const int d = static_cast<int>(idx - r * D);
+    const float lse = merged_lse(lses, n, rows, r);
+    float acc = 0.0f;
+    if (lse != -INFINITY) {
+      for (int c = 0; c < n; ++c) {
+        const float l = __ldg(lses + c * rows + r);
+        if (l == -INFINITY) continue;
+        acc = fmaf(__expf(l - lse), __ldg(partials + (c * rows + r) * D + d), acc);
+      }
+    }
+    out[idx] = acc;
+    if (lse_out != nullptr && d == 0) lse_out[r] = lse;
+  }
+}
+
+// out may alias eps_c or eps_u: every element is read and then written by
+// the same thread, so no __restrict__ here.
+__global__ void __launch_bounds__(kStreamThreads)
+    cfg_combine_vec4_kernel(const float4 *eps_c, const float4 *eps_u, float w, float4 *out, long long n4) {
+  const long long stride = static_cast<long long>(gridDim.x) * kStreamThreads;
+  for (long long i = static_cast<long long>(blockIdx.x) * kStreamThreads + threadIdx.x; i < n4; i += stride) {
+    const float4 c = ld_stream(eps_c + i);
+    const float4 u = ld_stream(eps_u + i);
+    float4 o;
+    o.x = fmaf(w, c.x - u.x, u.x);
+    o.y = fmaf(w, c.y - u.y, u.y);
+    o.z = fmaf(w, c.z - u.z, u.z);
+    o.w = fmaf(w, c.w - u.w, u.w);
+    st_stream(out + i, o);
+  }
+}
+
+__global__ void cfg_combine_tail_kernel(const float *eps_c, const float *eps_u, float w, float *out,
+                                        long long begin, long long numel) {
+  const long long i = begin + threadIdx.x;
+  if (i < numel) out[i] = fmaf(w, eps_c[i] - eps_u[i], eps_u[i]);
+}
+
+}  // namespace ditk

@@ -1,0 +1,120 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/dit_attn.h declares, and rejects bad arguments on the host (no call
+here reaches a kernel; the pointers below are never dereferenced)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from sequence_attention_attn_b300 import build, dit_attn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dit_attn.h")
+
+OK, INVALID, SHAPE, MISALIGNED = 0, -1, -2, -3
+
+# Fake, 16-byte aligned device addresses, far apart so that no range overlaps.
+A = 0x7F0000000000
+B_ = 0x7F1000000000
+C = 0x7F2000000000
+O = 0x7F3000000000
+L = 0x7F4000000000
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return dit_attn.lib()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text)) - {"defined"})
+
+
+def test_header_declares_the_boundary():
+    names = header_functions()
+    for want in ("dit_attn_fwd", "dit_attn_fwd_partials", "dit_attn_merge", "cfg_combine",
+                 "dit_last_device_status", "dit_status_string", "dit_abi_version"):
+        assert want in names
+
+
+def test_library_exports_every_header_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), f"{name} declared in dit_attn.h but not exported"
+    assert set(header_functions()) <= set(dit_attn.SIGNATURES)
+
+
+def test_status_strings(lib):
+    assert lib.dit_abi_version() == 1
+    for code in range(-7, 1):
+        s = dit_attn.status_string(code)
+        assert s and s != "unknown status"
+    assert dit_attn.status_string(-99) == "unknown status"
+
+
+def fwd(lib, q=A, k=B_, v=C, out=O, lse=L, B=1, H=2, S=256, D=64, n=1):
+    return lib.dit_attn_fwd(q, k, v, out, lse, B, H, S, D, n, None)
+
+
+def test_fwd_rejects_bad_arguments_on_host(lib):
+    assert fwd(lib, q=None) == INVALID
+    assert fwd(lib, out=None) == INVALID
+    assert fwd(lib, B=0) == INVALID
+    assert fwd(lib, H=-1) == INVALID
+    assert fwd(lib, S=0) == INVALID
+    assert fwd(lib, n=0) == INVALID
+    assert fwd(lib, n=257) == INVALID            # more chunks than keys
+    assert fwd(lib, D=65) == SHAPE
+    assert fwd(lib, D=96) == SHAPE
+    assert fwd(lib, q=A + 8) == MISALIGNED
+    assert fwd(lib, out=O + 4) == MISALIGNED
+    assert fwd(lib, lse=L + 2) == MISALIGNED
+    assert fwd(lib, out=A + 1024) == INVALID      # out overlaps q
+    assert fwd(lib, lse=O + 16) == INVALID        # lse overlaps out
+
+
+def test_partials_rejects_bad_arguments_on_host(lib):
+    f = lib.dit_attn_fwd_partials
+    assert f(A, B_, C, None, L, 1, 2, 256, 64, 2, None) == INVALID
+    assert f(A, B_, C, O, L + 4, 1, 2, 256, 64, 2, None) == MISALIGNED
+    assert f(A, B_, C, O, L, 1, 2, 256, 72, 300, None) == INVALID
+    assert f(A, B_, C, A, L, 1, 2, 256, 64, 2, None) == INVALID   # partials overlap q
+
+
+def test_merge_rejects_bad_arguments_on_host(lib):
+    f = lib.dit_attn_merge
+    assert f(None, B_, 2, O, L, 100, 64, None) == INVALID
+    assert f(A, B_, 0, O, L, 100, 64, None) == INVALID
+    assert f(A, B_, 2, O, L, 0, 64, None) == INVALID
+    assert f(A, B_, 2, O, L, 100, 0, None) == INVALID
+    assert f(A + 4, B_, 2, O, L, 100, 64, None) == MISALIGNED
+    assert f(A, B_, 2, A + 64, L, 100, 64, None) == INVALID        # out overlaps partials
+
+
+def test_cfg_rejects_bad_arguments_on_host(lib):
+    f = lib.cfg_combine
+    assert f(None, B_, 4.5, O, 100, None) == INVALID
+    assert f(A, B_, 4.5, O, 0, None) == INVALID
+    assert f(A, B_, float("nan"), O, 100, None) == INVALID
+    assert f(A, B_ + 4, 4.5, O, 100, None) == MISALIGNED
+    assert f(A, B_, 4.5, A + 16, 100, None) == INVALID             # partial overlap
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU behaviour")
+def test_valid_call_without_gpu_reports_an_error_not_a_result(lib):
+    # Arguments pass the host checks, so the library must reach the CUDA
+    # runtime, find no usable device and say so (no CPU fallback).
+    rc = fwd(lib)
+    assert rc in (-4, -7), rc
+
+
+def test_python_binding_refuses_cpu_tensors(lib):
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        dit_attn.attention(q, q, q)
+    with pytest.raises(ValueError, match="CUDA"):
+        dit_attn.combine(torch.zeros(4), torch.zeros(4), 1.0)

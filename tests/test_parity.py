@@ -1,0 +1,203 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle on the
+same seeded inputs (every workload, every chunk count it lists), plus edge
+cases (ragged tails, chunks shorter than a tile, S = 1, every head size)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity_util import (check_attention, check_f32, f64, oracle_rows, sample_rows)
+from sequence_attention_attn_b300 import dit_attn, workloads
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+def to_dev(*ts):
+    return [t.to(DEV) for t in ts]
+
+
+def assert_no_device_error():
+    assert dit_attn.dit_last_device_status() == 0, "a device-side wait ran out"
+
+
+# ------------------------------------------------------------ CFG combine
+@pytest.mark.parametrize("name", ["tiny", "pixart_1024"])
+def test_cfg_combine_workloads(name):
+    cfg = workloads.BY_NAME[name]
+    if name == "pixart_1024":
+        # one [2, 4, 128, 128] buffer: index 0 = cond, 1 = uncond
+        g = torch.Generator().manual_seed(workloads.seed_for(cfg, 100))
+        buf = torch.randn((2,) + cfg.cfg_shape, generator=g)
+        eps_c, eps_u = buf[0].contiguous(), buf[1].contiguous()
+    else:
+        eps_c, eps_u = workloads.make_cfg(cfg.cfg_shape, workloads.seed_for(cfg, 100))
+    ref = oracle.cfg_combine(eps_c.numpy(), eps_u.numpy(), cfg.cfg_w)
+    c, u = to_dev(eps_c, eps_u)
+    out = dit_attn.combine(c, u, cfg.cfg_w)
+    check_f32(out, ref, f"cfg {name}")
+    assert_no_device_error()
+
+
+@pytest.mark.parametrize("numel", [1, 3, 4, 5, 1023, 4096 + 3, 1 << 20])
+def test_cfg_combine_sizes_and_alias(numel):
+    eps_c, eps_u = workloads.make_cfg((numel,), 7 + numel)
+    ref = oracle.cfg_combine(eps_c.numpy(), eps_u.numpy(), 4.5)
+    c, u = to_dev(eps_c, eps_u)
+    check_f32(dit_attn.combine(c, u, 4.5), ref, f"cfg numel={numel}")
+    dit_attn.cfg_combine(c, u, 4.5, c)  # in place over eps_c
+    check_f32(c, ref, "cfg in place")
+    c1, u1 = to_dev(eps_c, eps_u)
+    check_f32(dit_attn.combine(c1, u1, 1.0), eps_c.double().numpy(), "w=1")
+    check_f32(dit_attn.combine(c1, u1, 0.0), eps_u.double().numpy(), "w=0")
+
+
+# ------------------------------------------------------------- LSE merge
+@pytest.mark.parametrize("n,rows,D", [(1, 100, 64), (2, 777, 72), (5, 300, 128), (16, 4096, 64),
+                                      (3, 50, 7), (16, 333, 1)])
+def test_merge_random(n, rows, D):
+    p, l = workloads.make_merge(n, rows, D, seed=n * 1000 + rows + D)
+    ref_o, ref_l = oracle.lse_merge(p.numpy(), l.numpy())
+    pd, ld = to_dev(p, l)
+    out, lse = dit_attn.merge(pd, ld)
+    check_f32(out, ref_o, f"merge O n={n} D={D}")
+    assert np.abs(f64(lse) - ref_l).max() <= 1e-5 * max(1.0, np.abs(ref_l).max())
+    assert_no_device_error()
+
+
+def test_merge_neg_inf_partials():
+    n, rows, D = 4, 513, 64
+    p, l = workloads.make_merge(n, rows, D, seed=5, neg_inf_frac=0.3)
+    l[:, :7] = float("-inf")                 # rows with no weight at all
+    p[1][torch.isinf(l[1])] = float("nan")   # never read when its LSE is -inf
+    ref_o, ref_l = oracle.lse_merge(p.numpy(), l.numpy())
+    pd, ld = to_dev(p, l)
+    out, lse = dit_attn.merge(pd, ld)
+    o = f64(out)
+    assert np.isfinite(o).all()
+    assert (o[:7] == 0).all() and np.isneginf(f64(lse)[:7]).all()
+    check_f32(o[7:], ref_o[7:], "merge with -inf")
+    fin = np.isfinite(ref_l)
+    assert np.abs(f64(lse)[fin] - ref_l[fin]).max() <= 1e-5 * max(1.0, np.abs(ref_l[fin]).max())
+
+
+def test_merge_video_workload_sampled():
+    cfg = workloads.BY_NAME["video"]
+    rows = cfg.rows
+    p, l = workloads.make_merge(cfg.merge_n, rows, cfg.D, seed=workloads.seed_for(cfg, 200),
+                                device=DEV)
+    out, lse = dit_attn.merge(p, l)
+    pick = sample_rows(1, rows, 2048, seed=3)
+    ref_o, ref_l = oracle.lse_merge(f64(p[:, pick]), f64(l[:, pick]))
+    check_f32(out[pick], ref_o, "video merge O")
+    assert np.abs(f64(lse[pick]) - ref_l).max() <= 1e-5 * max(1.0, np.abs(ref_l).max())
+    assert_no_device_error()
+
+
+# -------------------------------------------------------------- attention
+def run_attention(q, k, v, n):
+    qd, kd, vd = to_dev(q, k, v)
+    out, lse = dit_attn.attention(qd, kd, vd, n_kv_chunks=n)
+    torch.cuda.synchronize()
+    assert_no_device_error()
+    return out, lse
+
+
+@pytest.mark.parametrize("n", [1, 2, 4])
+def test_attention_tiny_full(n):
+    cfg = workloads.BY_NAME["tiny"]
+    q, k, v = workloads.make_qkv(cfg)
+    o_ref, l_ref = oracle.attention_chunked(f64(q), f64(k), f64(v), oracle.chunk_bounds(cfg.S, n))
+    out, lse = run_attention(q, k, v, n)
+    check_attention(out, lse, o_ref, l_ref, f"tiny n={n}")
+
+
+@pytest.mark.parametrize("n", [1, 2, 4, 8])
+def test_attention_dit_xl2_full(n):
+    cfg = workloads.BY_NAME["dit_xl2_512"]
+    q, k, v = workloads.make_qkv(cfg)
+    o_ref, l_ref = oracle.attention(f64(q), f64(k), f64(v))
+    out, lse = run_attention(q, k, v, n)
+    check_attention(out, lse, o_ref, l_ref, f"dit_xl2 n={n}")
+
+
+@pytest.mark.parametrize("name,n", [("pixart_1024", 1), ("pixart_1024", 4), ("pixart_1024", 8),
+                                    ("flux_mmdit", 1), ("flux_mmdit", 2), ("flux_mmdit", 4),
+                                    ("flux_mmdit", 8), ("video", 1), ("video", 8), ("video", 16)])
+def test_attention_full_size_sampled(name, n):
+    cfg = workloads.BY_NAME[name]
+    q, k, v = workloads.make_qkv(cfg)
+    out, lse = run_attention(q, k, v, n)
+    rows = sample_rows(cfg.B * cfg.H, cfg.S, 384, seed=cfg.index * 10 + n)
+    o_ref, l_ref = oracle_rows(q, k, v, rows)
+    D = cfg.D
+    check_attention(out.reshape(-1, D)[torch.as_tensor(rows, device=DEV)],
+                    lse.reshape(-1)[torch.as_tensor(rows, device=DEV)], o_ref, l_ref, f"{name} n={n}")
+
+
+@pytest.mark.parametrize("S", [1, 2, 100, 127, 128, 129, 255, 257, 383, 640])
+@pytest.mark.parametrize("D", [64, 72, 128])
+def test_attention_edge_lengths(S, D):
+    q, k, v = workloads.make_random_qkv(1, 3, S, D, seed=S * 7 + D, std=1.5)
+    o_ref, l_ref = oracle.attention(f64(q), f64(k), f64(v))
+    for n in sorted({1, min(S, 3), min(S, 7), S if S <= 16 else 16}):
+        out, lse = run_attention(q, k, v, n)
+        check_attention(out, lse, o_ref, l_ref, f"S={S} D={D} n={n}", scaled=True)
+
+
+def test_attention_chunks_shorter_than_a_tile():
+    # 40 chunks of 6-7 keys: every tile is cut at a chunk end
+    q, k, v = workloads.make_random_qkv(2, 2, 260, 64, seed=99, std=2.0)
+    o_ref, l_ref = oracle.attention(f64(q), f64(k), f64(v))
+    out, lse = run_attention(q, k, v, 40)
+    check_attention(out, lse, o_ref, l_ref, "n=40", scaled=True)
+    out, lse = run_attention(q, k, v, 260)   # one key per chunk
+    check_attention(out, lse, o_ref, l_ref, "n=S", scaled=True)
+
+
+def test_attention_sharp_softmax():
+    # large logits: the reference max moves often and by a lot
+    q, k, v = workloads.make_random_qkv(1, 4, 512, 128, seed=5, std=4.0)
+    o_ref, l_ref = oracle.attention(f64(q), f64(k), f64(v))
+    for n in (1, 3):
+        out, lse = run_attention(q, k, v, n)
+        check_attention(out, lse, o_ref, l_ref, f"sharp n={n}", scaled=True)
+
+
+def test_attention_without_lse_output():
+    q, k, v = workloads.make_random_qkv(1, 2, 300, 72, seed=8)
+    o_ref, _ = oracle.attention(f64(q), f64(k), f64(v))
+    qd, kd, vd = to_dev(q, k, v)
+    out, lse = dit_attn.attention(qd, kd, vd, 2, with_lse=False)
+    assert lse is None
+    check_attention(out, None, o_ref, None, "no lse")
+
+
+# ------------------------------------------------- partials + standalone merge
+@pytest.mark.parametrize("name,n", [("tiny", 2), ("tiny", 4), ("dit_xl2_512", 8)])
+def test_partials_then_merge(name, n):
+    cfg = workloads.BY_NAME[name]
+    q, k, v = workloads.make_qkv(cfg)
+    qd, kd, vd = to_dev(q, k, v)
+    parts, lses = dit_attn.attention_partials(qd, kd, vd, n)
+    torch.cuda.synchronize()
+    assert_no_device_error()
+    qf, kf, vf = f64(q), f64(k), f64(v)
+    for c, (j0, j1) in enumerate(oracle.chunk_bounds(cfg.S, n)):
+        o_c, l_c = oracle.attention(qf, kf, vf, j0, j1)
+        check_attention(parts[c], lses[c], o_c.reshape(-1, cfg.D), l_c.reshape(-1), f"{name} chunk {c}")
+    out, lse = dit_attn.merge(parts, lses)
+    o_ref, l_ref = oracle.attention(qf, kf, vf)
+    check_attention(out, lse, o_ref.reshape(-1, cfg.D), l_ref.reshape(-1), f"{name} merged")
+    # the merge of the GPU partials is exactly the oracle merge of those partials
+    m_ref, ml_ref = oracle.lse_merge(f64(parts), f64(lses))
+    check_f32(out, m_ref, f"{name} merge of gpu partials")
+
+
+def test_repeatable_bitwise():
+    cfg = workloads.BY_NAME["tiny"]
+    q, k, v = to_dev(*workloads.make_qkv(cfg))
+    a, la = dit_attn.attention(q, k, v, 2)
+    b, lb = dit_attn.attention(q, k, v, 2)
+    assert torch.equal(a, b) and torch.equal(la, lb)
