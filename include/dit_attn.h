@@ -136,6 +136,17 @@ dit_status cfg_combine(const float *eps_c, const float *eps_u, float w,
  */
 dit_status dit_last_device_status(dit_stream_t stream);
 
+/*
+ * dit_selftest_bounded_wait -- exercises the failure path of the bounded
+ * device-side waits: launches one thread that waits on a shared-memory
+ * mbarrier nothing ever arrives on.  After about one second the wait gives up,
+ * sets the status word and the kernel returns normally (no trap, no fault; the
+ * context stays usable).  The next dit_last_device_status() on the same
+ * stream then returns DIT_ERR_DEVICE_TIMEOUT.  Diagnostic only; the pages
+ * have no counterpart (they detect slow devices at the scheduling level).
+ */
+dit_status dit_selftest_bounded_wait(dit_stream_t stream);
+
 /* Static English text for a status code; never NULL. */
 const char *dit_status_string(dit_status status);
 

@@ -448,16 +448,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           for (int j = 0; j < kBlockN; ++j)
             if (j >= valid) sr[j] = __float_as_uint(-INFINITY);
         }
-        float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
-        float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
+        // Row max: eight independent chains of 3-input max.
+        float mx[8];
 #pragma unroll
-        for (int j = 4; j < kBlockN; j += 4) {
-          mx0 = fmaxf(mx0, __uint_as_float(sr[j + 0]));
-          mx1 = fmaxf(mx1, __uint_as_float(sr[j + 1]));
-          mx2 = fmaxf(mx2, __uint_as_float(sr[j + 2]));
-          mx3 = fmaxf(mx3, __uint_as_float(sr[j + 3]));
+        for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(sr[i]);
+#pragma unroll
+        for (int j = 8; j < kBlockN; j += 16) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            mx[i] = max3(mx[i], __uint_as_float(sr[j + i]), __uint_as_float(sr[j + 8 + i]));
         }
-        const float tmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * scale_log2;
+        const float tmax =
+            max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * scale_log2;
         float o_scale = 1.0f;
         if (kv.chunk_start() && it > 0) {
           // The previous chunk is complete: fold its LSE into the running one.
@@ -472,23 +474,33 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           l *= f;
           m = tmax;
         }
-        if (it > 0 && __any_sync(0xffffffffu, o_scale != 1.0f)) rescale_o<D>(tO, o_scale);
         const float neg_m = -m;
-        float sum0 = 0.0f, sum1 = 0.0f;
+        // P = 2^(S * scale - m): the affine part on packed pairs, 2^x on the
+        // MUFU, row sum in four packed accumulators, P packed to bf16 pairs.
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int qtr = 0; qtr < 4; ++qtr) {
           uint32_t pr[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const float a = ex2_approx(fmaf(__uint_as_float(sr[qtr * 32 + 2 * j]), scale_log2, neg_m));
-            const float b = ex2_approx(fmaf(__uint_as_float(sr[qtr * 32 + 2 * j + 1]), scale_log2, neg_m));
-            sum0 += a;
-            sum1 += b;
+            float x0, x1;
+            fma2(x0, x1, __uint_as_float(sr[qtr * 32 + 2 * j]), __uint_as_float(sr[qtr * 32 + 2 * j + 1]),
+                 scale_log2, scale_log2, neg_m, neg_m);
+            const float a = ex2_approx(x0);
+            const float b = ex2_approx(x1);
+            add2(acc[2 * (j & 3)], acc[2 * (j & 3) + 1], a, b);
             pr[j] = pack_bf16x2(a, b);
           }
           tmem_st16(tS + qtr * 16, pr);
         }
-        l += sum0 + sum1;
+        add2(acc[0], acc[1], acc[2], acc[3]);
+        add2(acc[4], acc[5], acc[6], acc[7]);
+        add2(acc[0], acc[1], acc[4], acc[5]);
+        l += acc[0] + acc[1];
+        // O may be rescaled after P is written: the PV MMA that reads both waits
+        // for this warpgroup's arrival below.  Doing it here, once the S values
+        // are dead, keeps the row in registers without spilling.
+        if (it > 0 && __any_sync(0xffffffffu, o_scale != 1.0f)) rescale_o<D>(tO, o_scale);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(p_full(t));

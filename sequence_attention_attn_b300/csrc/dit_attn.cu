@@ -322,6 +322,15 @@ dit_status cfg_combine(const float *eps_c, const float *eps_u, float w, float *o
   return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ERR_LAUNCH;
 }
 
+dit_status dit_selftest_bounded_wait(dit_stream_t stream) {
+  int dev = 0;
+  DeviceState *st = nullptr;
+  dit_status s = select_device(stream, &dev, &st);
+  if (s != DIT_OK) return s;
+  ditk::selftest_wait_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>();
+  return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ERR_LAUNCH;
+}
+
 dit_status dit_last_device_status(dit_stream_t stream) {
   int dev = 0;
   DeviceState *st = nullptr;

@@ -35,6 +35,7 @@ SIGNATURES = {
                        ctypes.c_int),
     "cfg_combine": ([_vp, _vp, ctypes.c_float, _vp, ctypes.c_longlong, _vp], ctypes.c_int),
     "dit_last_device_status": ([_vp], ctypes.c_int),
+    "dit_selftest_bounded_wait": ([_vp], ctypes.c_int),
     "dit_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "dit_abi_version": ([], ctypes.c_int),
 }
@@ -163,6 +164,11 @@ def cfg_combine(eps_c, eps_u, w: float, out, stream=None) -> None:
 def dit_last_device_status(stream=None) -> int:
     """Synchronise the stream, read and clear the device status word."""
     return int(lib().dit_last_device_status(_stream(stream)))
+
+
+def dit_selftest_bounded_wait(stream=None) -> None:
+    """Launch the bounded-wait self test (its wait runs out after ~1 s)."""
+    _check(lib().dit_selftest_bounded_wait(_stream(stream)), "dit_selftest_bounded_wait")
 
 
 # --------------------------------------------------------- conveniences

@@ -5,9 +5,8 @@ Tolerances:
   attention LSE           max-abs <= 1e-3
   fp32 merge / CFG        max-abs <= 1e-5 * max|ref| (norm-wise relative)
 
-The attention bounds are absolute for outputs of magnitude <= 1, which is
-what every workload produces (checked: ``scaled=False`` also asserts it).
-Edge-case inputs drawn with a larger spread give outputs up to ~20, where
+The attention bounds are absolute and are applied as such to every workload
+(``scaled=False``).  Edge-case inputs drawn with a larger spread give outputs up to ~20, where
 bf16 itself cannot hold 2e-2 (half an ulp at 16 is 0.0625): bf16 rounding of
 the output and of the largest probability each cost up to 2^-9 of the output
 scale.  For those (``scaled=True``) the bounds are multiplied by
@@ -36,8 +35,6 @@ def check_attention(o_gpu, lse_gpu, o_ref, lse_ref, what="", scaled=False):
     assert np.isfinite(o).all(), f"{what}: non-finite output"
     max_scale = max(1.0, float(np.abs(o_ref).max())) if scaled else 1.0
     mean_scale = max(1.0, float(np.abs(o_ref).mean())) if scaled else 1.0
-    if not scaled:
-        assert np.abs(o_ref).max() <= 1.0 + 1e-9, f"{what}: |O| > 1, use scaled bounds"
     assert err.max() <= O_MAX_ABS * max_scale, f"{what}: O max-abs {err.max():.3e}"
     assert err.mean() <= O_MEAN_ABS * mean_scale, f"{what}: O mean-abs {err.mean():.3e}"
     if lse_gpu is not None:

@@ -201,3 +201,20 @@ def test_repeatable_bitwise():
     a, la = dit_attn.attention(q, k, v, 2)
     b, lb = dit_attn.attention(q, k, v, 2)
     assert torch.equal(a, b) and torch.equal(la, lb)
+
+
+def test_bounded_wait_times_out_without_fault():
+    """A wait that nothing satisfies gives up after ~1 s: the kernel returns,
+    the status word reports the timeout once, and the context stays usable."""
+    import time
+    assert dit_attn.dit_last_device_status() == 0
+    t0 = time.perf_counter()
+    dit_attn.dit_selftest_bounded_wait()
+    assert dit_attn.dit_last_device_status() == -6      # DIT_ERR_DEVICE_TIMEOUT
+    assert time.perf_counter() - t0 < 30.0
+    assert dit_attn.dit_last_device_status() == 0       # read-and-clear
+    cfg = workloads.BY_NAME["tiny"]
+    q, k, v = workloads.make_qkv(cfg)
+    o_ref, l_ref = oracle.attention(f64(q), f64(k), f64(v))
+    out, lse = run_attention(q, k, v, 2)                # still works afterwards
+    check_attention(out, lse, o_ref, l_ref, "after timeout")
