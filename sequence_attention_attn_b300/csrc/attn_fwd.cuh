@@ -58,37 +58,40 @@ constexpr float kLog2e = 1.442695040888963407f;
 
 // Per head-dimension layout.  The head dimension is the MMA K of QK^T and the
 // MMA N of PV.  Columns 0..63 live in a 128-byte-swizzled block; the rest in a
-// second block: 64 columns (D = 128, 128-byte swizzle) or 16 columns (D = 72,
-// 32-byte swizzle; columns 72..79 are zero-filled by TMA, so padding to 80 is
-// exact).
+// second block: 64 columns (D = 128, 128-byte swizzle) or, for Q and K with
+// D = 72, 16 columns (32-byte swizzle; one more K = 16 step of QK^T).  V with
+// D = 72 carries a full 128-byte-swizzled block from column 64, so that PV is
+// a single N = 80 MMA per 16 keys.  TMA zero-fills every column past 71, so
+// padding D to 80 is exact.
 template <int D>
 struct AttnCfg;
 template <>
 struct AttnCfg<64> {
-  static constexpr int kDpad = 64, kTail = 0, kStages = 4;
+  static constexpr int kDpad = 64, kTail = 0, kVTail = 0, kStages = 4;
 };
 template <>
 struct AttnCfg<72> {
-  static constexpr int kDpad = 80, kTail = 16, kStages = 4;
+  static constexpr int kDpad = 80, kTail = 16, kVTail = 64, kStages = 3;
 };
 template <>
 struct AttnCfg<128> {
-  static constexpr int kDpad = 128, kTail = 64, kStages = 2;
+  static constexpr int kDpad = 128, kTail = 64, kVTail = 64, kStages = 2;
 };
 
 template <int D>
 struct AttnLayout {
   using C = AttnCfg<D>;
-  static constexpr int kTileBytes = kSwzBytes + kBlockM * C::kTail * 2;
+  static constexpr int kTileBytes = kSwzBytes + kBlockM * C::kTail * 2;    // a Q or K tile
+  static constexpr int kVTileBytes = kSwzBytes + kBlockM * C::kVTail * 2;  // a V tile
   static constexpr int kQOff = 0;
   static constexpr int kKOff = 2 * kTileBytes;
   static constexpr int kVOff = kKOff + C::kStages * kTileBytes;
-  static constexpr int kBarOff = kVOff + C::kStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + C::kStages * kVTileBytes;
   static constexpr int kNumBars = 2 + 4 * C::kStages + 7;
   static constexpr int kTmemSlotOff = kBarOff + 8 * kNumBars;
   static constexpr int kBytes = kTmemSlotOff + 16;
   static constexpr int kSmemLaunch = kBytes + 1024;  // slack for 1024-byte alignment
-  static_assert(kTileBytes % 1024 == 0, "tiles must keep 1024-byte alignment");
+  static_assert(kTileBytes % 1024 == 0 && kVTileBytes % 1024 == 0, "tiles must keep 1024-byte alignment");
   static_assert(kSmemLaunch <= 232448, "shared memory budget");
 };
 
@@ -163,25 +166,14 @@ __device__ __forceinline__ void issue_qk(uint32_t tS, uint32_t q_smem, uint32_t 
 // shared memory (rows = keys, 128 bytes per row per 64-column block).
 template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_smem, bool accumulate) {
-  if constexpr (D == 72) {
-    constexpr uint32_t idesc_main = idesc_bf16_f32(kBlockM, 64, true);
-    constexpr uint32_t idesc_tail = idesc_bf16_f32(kBlockM, 16, true);
+  // One MMA of N = Dpad per 16 keys; the leading byte offset steps from one
+  // 64-column block of V to the next.
+  constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, AttnCfg<D>::kDpad, true);
 #pragma unroll
-    for (int ks = 0; ks < kBlockN / 16; ++ks) {
-      const uint32_t acc = (accumulate || ks > 0) ? 1u : 0u;
-      const uint64_t b0 = smem_desc(v_smem + ks * 2048, kSwzBytes, 1024, kSwizzle128B);
-      umma_ts(tO, tP + ks * 8, b0, idesc_main, acc);
-      const uint64_t b1 = smem_desc(v_smem + kSwzBytes + ks * 512, 4096, 256, kSwizzle32B);
-      umma_ts(tO + 64, tP + ks * 8, b1, idesc_tail, acc);
-    }
-  } else {
-    constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, AttnCfg<D>::kDpad, true);
-#pragma unroll
-    for (int ks = 0; ks < kBlockN / 16; ++ks) {
-      const uint32_t acc = (accumulate || ks > 0) ? 1u : 0u;
-      const uint64_t b = smem_desc(v_smem + ks * 2048, kSwzBytes, 1024, kSwizzle128B);
-      umma_ts(tO, tP + ks * 8, b, idesc, acc);
-    }
+  for (int ks = 0; ks < kBlockN / 16; ++ks) {
+    const uint32_t acc = (accumulate || ks > 0) ? 1u : 0u;
+    const uint64_t b = smem_desc(v_smem + ks * 2048, kSwzBytes, 1024, kSwizzle128B);
+    umma_ts(tO, tP + ks * 8, b, idesc, acc);
   }
 }
 
@@ -240,6 +232,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   using L = AttnLayout<D>;
   constexpr int NS = C::kStages;
   constexpr uint32_t kTileBytes = L::kTileBytes;
+  constexpr uint32_t kVTileBytes = L::kVTileBytes;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
@@ -350,10 +343,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if constexpr (C::kTail > 0) tma_load_3d(kd + kSwzBytes, &tm_k_tail, k_full(s), 64, kv.t0, bh, pol_kv);
         k_last[s] = u;
         if (u > 0 && !mbar_wait(v_empty(s), (u - 1) & 1)) break;
-        const uint32_t vd = sV0 + s * kTileBytes;
-        mbar_arrive_expect_tx(v_full(s), kTileBytes);
+        const uint32_t vd = sV0 + s * kVTileBytes;
+        mbar_arrive_expect_tx(v_full(s), kVTileBytes);
         tma_load_3d(vd, &tm_v, v_full(s), 0, kv.t0, bh, pol_kv);
-        if constexpr (C::kTail > 0) tma_load_3d(vd + kSwzBytes, &tm_v_tail, v_full(s), 64, kv.t0, bh, pol_kv);
+        if constexpr (C::kVTail > 0) tma_load_3d(vd + kSwzBytes, &tm_v_tail, v_full(s), 64, kv.t0, bh, pol_kv);
         v_last[s] = u;
         kv.next();
       }
@@ -381,7 +374,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc_fence_after();
         const uint32_t ks = sK0 + s * kTileBytes;
         const int ps = (it + NS - 1) % NS;
-        const uint32_t vs = sV0 + ps * kTileBytes;
+        const uint32_t vs = sV0 + ps * kVTileBytes;
         if (it > 0) {
           if (!(ok = mbar_wait(p_full(0), (it - 1) & 1))) break;
           if (!(ok = mbar_wait(v_full(ps), ((it - 1) / NS) & 1))) break;
@@ -404,7 +397,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       if (ok) {
         const int ls = (tiles - 1) % NS;
-        const uint32_t vs = sV0 + ls * kTileBytes;
+        const uint32_t vs = sV0 + ls * kVTileBytes;
         ok = mbar_wait(p_full(0), (tiles - 1) & 1) && mbar_wait(v_full(ls), ((tiles - 1) / NS) & 1);
         if (ok) {
           tc_fence_after();

@@ -132,15 +132,18 @@ dit_status launch_attn(DeviceState &st, int didx, const void *q, const void *k, 
   if ((s = encode_qkv_map(&mq, q, BH, S, D, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != DIT_OK) return s;
   if ((s = encode_qkv_map(&mk, k, BH, S, D, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != DIT_OK) return s;
   if ((s = encode_qkv_map(&mv, v, BH, S, D, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != DIT_OK) return s;
+  // Columns 64.. of Q and K: a 16-column 32-byte-swizzled box for D = 72 (the
+  // last K step of QK^T), the main map's 64-column box otherwise.  V always
+  // takes the main map's box at column 64 (D = 72: columns 72..127 of that box
+  // are zero-filled, and PV runs with N = 80).
   if (D == 72) {
     if ((s = encode_qkv_map(&mq_t, q, BH, S, D, 16, CU_TENSOR_MAP_SWIZZLE_32B)) != DIT_OK) return s;
     if ((s = encode_qkv_map(&mk_t, k, BH, S, D, 16, CU_TENSOR_MAP_SWIZZLE_32B)) != DIT_OK) return s;
-    if ((s = encode_qkv_map(&mv_t, v, BH, S, D, 16, CU_TENSOR_MAP_SWIZZLE_32B)) != DIT_OK) return s;
   } else {
     mq_t = mq;
     mk_t = mk;
-    mv_t = mv;
   }
+  mv_t = mv;
   kernel<<<grid, ditk::kAttnThreads, L::kSmemLaunch, stream>>>(mq, mq_t, mk, mk_t, mv, mv_t, prm);
   return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ERR_LAUNCH;
 }
