@@ -53,6 +53,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="video")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="override the head count (a smaller case of the same workload, for profiling)")
     ap.add_argument("--chunks", type=int, default=None, help="n_kv_chunks (default: the workload's largest)")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
@@ -215,8 +217,7 @@ def run_reference(args):
     rank, world, _local = dist_env()
     if rank != 0:
         return 0
-    from sequence_attention_attn_b300 import workloads
-    cfg = workloads.BY_NAME[args.workload]
+    cfg = select_workload(args)
     n = args.chunks or cfg.merge_n or max(cfg.chunk_counts)
     per_step = max(0.5, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
     flops, dt, desc, threads = cpu_oracle_sample(cfg, per_step)
@@ -266,6 +267,18 @@ def workload_config(cfg, n):
 
 
 # ------------------------------------------------------------ our arm
+def select_workload(args):
+    """The named workload, with the head count overridden if --heads is given."""
+    import dataclasses
+    from sequence_attention_attn_b300 import workloads
+    cfg = workloads.BY_NAME[args.workload]
+    if args.heads is not None:
+        if args.heads < 1:
+            raise SystemExit("--heads must be >= 1")
+        cfg = dataclasses.replace(cfg, H=args.heads)
+    return cfg
+
+
 def run_ours(args):
     import torch
     rank, world, local = dist_env()
@@ -276,7 +289,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
 
     from sequence_attention_attn_b300 import dit_attn, workloads
-    cfg = workloads.BY_NAME[args.workload]
+    cfg = select_workload(args)
     n = args.chunks or cfg.merge_n or max(cfg.chunk_counts)
     peaks, peak_src = load_peaks()
 
