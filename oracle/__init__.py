@@ -102,6 +102,9 @@ class OracleLib:
         lib.oracle_cfg_combine.argtypes = [_dptr, _dptr, ctypes.c_double, _dptr,
                                            ctypes.c_longlong]
         lib.oracle_cfg_combine.restype = ctypes.c_int
+        lib.oracle_cfg_relmae.argtypes = [_dptr, _dptr, ctypes.c_double, _dptr,
+                                          ctypes.c_longlong, _dptr]
+        lib.oracle_cfg_relmae.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
         self._lib = lib
@@ -164,6 +167,17 @@ class OracleLib:
         self._lib.oracle_cfg_combine(_p(eps_c), _p(eps_u), float(w), _p(out), eps_c.size)
         return out
 
+    def cfg_relmae(self, eps_c, eps_u, w: float):
+        """CFG combine plus the rel-MAE sums.  Returns (out, (sum |eps_c - eps_u|,
+        sum |eps_u|)); the rel-MAE is their ratio."""
+        eps_c, eps_u = _as_f64(eps_c), _as_f64(eps_u)
+        if eps_c.shape != eps_u.shape:
+            raise ValueError("eps_c and eps_u must share one shape")
+        out = np.empty_like(eps_c)
+        sums = np.zeros(2, dtype=np.float64)
+        self._lib.oracle_cfg_relmae(_p(eps_c), _p(eps_u), float(w), _p(out), eps_c.size, _p(sums))
+        return out, (float(sums[0]), float(sums[1]))
+
     def attention_chunked(self, q, k, v, bounds):
         """Chunked attention: (O_c, LSE_c) per key range in ``bounds``, then the
         log-sum-exp merge.  Returns (O, LSE) shaped like ``attention``."""
@@ -220,6 +234,10 @@ def lse_merge(partials, lses):
 
 def cfg_combine(eps_c, eps_u, w: float):
     return default().cfg_combine(eps_c, eps_u, w)
+
+
+def cfg_relmae(eps_c, eps_u, w: float):
+    return default().cfg_relmae(eps_c, eps_u, w)
 
 
 def attention_chunked(q, k, v, bounds):

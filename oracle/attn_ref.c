@@ -32,6 +32,13 @@
  *    Data-Pipeline Parallelism Based on Conditional Guidance Scheduling",
  *    Technische Zusammenfassung 2A: the path with prompt c and the path with
  *    c = empty), in its standard form out = eps_u + w (eps_c - eps_u).
+ *  - The discrepancy between the two paths that the same page (section 2B,
+ *    adaptive parallelism switching) measures to pick its phase switch points,
+ *    named rel-MAE there without a formula.  Plainest reading: the mean
+ *    absolute difference relative to the mean absolute unconditional noise,
+ *        rel-MAE = sum_i |eps_c[i] - eps_u[i]| / sum_i |eps_u[i]|,
+ *    computed in the same pass as the combine; the two sums are returned and
+ *    their ratio is the rel-MAE.
  *
  * Layouts: q, k, v, out are [BH][S][D] row-major doubles; lse is [BH][S].
  * Every loop is the definition written out, with no blocking or reordering.
@@ -155,6 +162,23 @@ int oracle_cfg_combine(const double *eps_c, const double *eps_u, double w,
 #pragma omp parallel for schedule(static)
   for (long long i = 0; i < numel; ++i)
     out[i] = eps_u[i] + w * (eps_c[i] - eps_u[i]);
+  return 0;
+}
+
+/* Classifier-free guidance combine plus the two sums of the rel-MAE
+ * discrepancy: sums[0] = sum |eps_c - eps_u|, sums[1] = sum |eps_u|. */
+int oracle_cfg_relmae(const double *eps_c, const double *eps_u, double w,
+                      double *out, long long numel, double *sums) {
+  if (numel < 0) return -1;
+  double diff = 0.0, base = 0.0;
+  for (long long i = 0; i < numel; ++i) {
+    const double d = eps_c[i] - eps_u[i];
+    out[i] = eps_u[i] + w * d;
+    diff += fabs(d);
+    base += fabs(eps_u[i]);
+  }
+  sums[0] = diff;
+  sums[1] = base;
   return 0;
 }
 

@@ -44,3 +44,10 @@ def cfg_combine(eps_c, eps_u, w):
     eps_c = np.asarray(eps_c, dtype=np.float64)
     eps_u = np.asarray(eps_u, dtype=np.float64)
     return (1.0 - w) * eps_u + w * eps_c
+
+
+def relmae_sums(eps_c, eps_u):
+    """(sum |eps_c - eps_u|, sum |eps_u|) with NumPy's pairwise summation."""
+    eps_c = np.asarray(eps_c, dtype=np.float64)
+    eps_u = np.asarray(eps_u, dtype=np.float64)
+    return float(np.abs(eps_c - eps_u).sum()), float(np.abs(eps_u).sum())

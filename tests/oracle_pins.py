@@ -214,6 +214,33 @@ def pin_cfg(impl):
     _close(impl.cfg_combine(ec, eu, 4.5), brute.cfg_combine(ec, eu, 4.5), what="twin")
 
 
+def pin_cfg_relmae(impl):
+    """rel-MAE sums: exact values on integer inputs (every partial sum is an
+    exact integer in fp64); eps_c = eps_u gives 0, eps_c = 2 eps_u gives a
+    ratio of exactly 1, eps_c = -eps_u exactly 2; the ratio is scale
+    invariant; the fused combine equals the plain one; the sums match the
+    NumPy twin."""
+    u = np.array([1.0, -2.0, 3.0, -4.0])
+    c = np.array([2.0, 0.0, 3.0, 1.0])          # |c - u| = 1, 2, 0, 5
+    _, (d, b) = impl.cfg_relmae(c, u, 4.5)
+    assert (d, b) == (8.0, 10.0), (d, b)
+    rng = np.random.default_rng(24)
+    u = _rand(rng, 3, 16, 16)
+    _, (d, b) = impl.cfg_relmae(u, u, 2.0)
+    assert d == 0.0 and b > 0.0
+    _, (d, b) = impl.cfg_relmae(2.0 * u, u, 2.0)
+    assert d == b, (d, b)
+    _, (d, b) = impl.cfg_relmae(-u, u, 2.0)
+    assert d == 2.0 * b, (d, b)
+    c = _rand(rng, 3, 16, 16)
+    out, (d, b) = impl.cfg_relmae(c, u, 4.5)
+    _, (d3, b3) = impl.cfg_relmae(3.0 * c, 3.0 * u, 4.5)
+    _close(d3 / b3, d / b, what="scale invariance")
+    _close(out, impl.cfg_combine(c, u, 4.5), what="fused combine")
+    db, bb = brute.relmae_sums(c, u)
+    _close([d, b], [db, bb], what="twin")
+
+
 def pin_one_hot(impl):
     """One key whose score exceeds every other by more than 55 takes all the
     weight: O equals its value row to within exp(-55) relative."""
@@ -244,5 +271,5 @@ PINS = [
     pin_brute_twin, pin_single_key, pin_zero_query, pin_constant_v,
     pin_shift_invariance, pin_permutation, pin_two_key_logistic,
     pin_chunked_equals_unchunked, pin_merge_identities, pin_merge_brute,
-    pin_merge_neg_inf, pin_cfg, pin_one_hot, pin_rows_match_full,
+    pin_merge_neg_inf, pin_cfg, pin_cfg_relmae, pin_one_hot, pin_rows_match_full,
 ]

@@ -36,6 +36,10 @@ MUTANTS = [
      "out[i] = eps_c[i] + w * (eps_c[i] - eps_u[i]);"),
     ("key_range_off_by_one", "for (long long j = j0; j < j1; ++j) z +=",
      "for (long long j = j0 + 1; j < j1; ++j) z +="),
+    ("relmae_base_of_cond", "base += fabs(eps_u[i]);", "base += fabs(eps_c[i]);"),
+    ("relmae_signed_difference", "diff += fabs(d);", "diff += d;"),
+    ("relmae_difference_of_base", "diff += fabs(d);", "diff += fabs(eps_u[i]);"),
+    ("relmae_combine_sign", "out[i] = eps_u[i] + w * d;", "out[i] = eps_u[i] - w * d;"),
 ]
 
 
