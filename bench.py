@@ -316,7 +316,7 @@ def run_ours(args):
         dit_attn.dit_attn_merge(parts, part_lse, m_out, m_lse, sptr)
         dit_attn.cfg_combine(eps_c, eps_u, cfg.cfg_w, c_out, sptr)
 
-    launches_per_step = 2 + (1 if eps_c.numel() % 4 == 0 else 2)
+    launches_per_step = 2 + (1 if eps_c.numel() % 4 == 0 else 2)  # attention, merge, CFG (+ its tail)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -368,6 +368,8 @@ def run_ours(args):
     e2e = run_e2e(args, q, k, v, parts, part_lse, eps_c, eps_u, out, lse, m_out, m_lse, c_out, n, cfg,
                   world, dev)
 
+    hbm_cfg = cfg_hbm_sweep(peaks, dev)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         f, dt, desc, threads = cpu_oracle_sample(cfg, args.cpu_seconds)
@@ -394,6 +396,7 @@ def run_ours(args):
             "cfg_combine": {"ms": cfg_ms, "bytes": cfg_bytes, "gbs": cfg_bytes / (cfg_ms / 1e3) / 1e9,
                             "note": "latent pair fits in L2; launch-bound"},
         },
+        "cfg_hbm": hbm_cfg,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,
@@ -405,6 +408,40 @@ def run_ours(args):
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def cfg_hbm_sweep(peaks, dev, numel=1 << 26, reps=10):
+    """The CFG combine and its rel-MAE-fused form on operands larger than L2
+    (2^26 fp32 elements each: 768 MB of algorithmic traffic per call), outside
+    the timed step: the bandwidth figure the workload latents (L2-resident)
+    cannot show."""
+    import torch
+    from sequence_attention_attn_b300 import dit_attn
+    g = torch.Generator(device=dev).manual_seed(5)
+    c = torch.randn(numel, generator=g, device=dev)
+    u = torch.randn(numel, generator=g, device=dev)
+    o = torch.empty_like(c)
+    sums = torch.empty(2, dtype=torch.float64, device=dev)
+    stream = torch.cuda.current_stream()
+    res = {"numel_per_operand": numel, "bytes_per_call": 12.0 * numel, "l2": "operands larger than L2; no flush"}
+    for name, fn in (("cfg_combine", lambda: dit_attn.cfg_combine(c, u, 4.5, o, stream.cuda_stream)),
+                     ("cfg_combine_relmae", lambda: dit_attn.cfg_combine_relmae(c, u, 4.5, o, sums,
+                                                                                stream.cuda_stream))):
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        gbs = 12.0 * numel / (ms / 1e3) / 1e9
+        res[name] = {"ms": ms, "gbs": gbs, "frac_of_measured_hbm": gbs / peaks["hbm_gbs"],
+                     "frac_of_nominal_8000": gbs / NOMINAL_HBM_GBS}
+    res["rel_mae"] = float(sums[0] / sums[1])
+    del c, u, o
+    return res
 
 
 def run_e2e(args, q, k, v, parts, part_lse, eps_c, eps_u, out, lse, m_out, m_lse, c_out, n, cfg, world, dev):

@@ -129,6 +129,26 @@ dit_status cfg_combine(const float *eps_c, const float *eps_u, float w,
                        float *out, long long numel, dit_stream_t stream);
 
 /*
+ * cfg_combine_relmae -- cfg_combine fused with the discrepancy between the two
+ * guidance paths, measured in the same pass.  Source: "Accelerating Diffusion
+ * via Hybrid Data-Pipeline Parallelism Based on Conditional Guidance
+ * Scheduling" (Technische Zusammenfassung 2B: the switch points between its
+ * three phases are chosen from the rel-MAE between the conditional and the
+ * unconditional noise; the page gives no formula, the reading taken is
+ * sum |eps_c - eps_u| / sum |eps_u|).
+ *
+ *   eps_c, eps_u, out, numel, w   as for cfg_combine (out may alias an input).
+ *   sums   fp64 [2] device, 8-byte aligned, not overlapping the other buffers:
+ *          set to {sum |eps_c - eps_u|, sum |eps_u|} (zeroed by this call
+ *          before the kernel runs); the rel-MAE is sums[0] / sums[1].  The
+ *          sums are accumulated in fp32 per thread and fp64 beyond, in an order
+ *          that may vary between calls in the last bits.
+ */
+dit_status cfg_combine_relmae(const float *eps_c, const float *eps_u, float w,
+                              float *out, long long numel, double *sums,
+                              dit_stream_t stream);
+
+/*
  * dit_last_device_status -- synchronises `stream`, then reads and clears this
  * device's status word.  Returns DIT_ERR_DEVICE_TIMEOUT if a kernel gave up on
  * a bounded wait since the last call, DIT_ERR_CUDA if the synchronisation

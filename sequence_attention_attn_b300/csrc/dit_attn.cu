@@ -325,6 +325,31 @@ dit_status cfg_combine(const float *eps_c, const float *eps_u, float w, float *o
   return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ERR_LAUNCH;
 }
 
+dit_status cfg_combine_relmae(const float *eps_c, const float *eps_u, float w, float *out, long long numel,
+                              double *sums, dit_stream_t stream) {
+  if (eps_c == nullptr || eps_u == nullptr || out == nullptr || sums == nullptr) return DIT_ERR_INVALID_ARG;
+  if (numel < 1 || numel > (1LL << 46)) return DIT_ERR_INVALID_ARG;
+  if (!std::isfinite(w)) return DIT_ERR_INVALID_ARG;
+  if (!aligned16(eps_c) || !aligned16(eps_u) || !aligned16(out) || (reinterpret_cast<uintptr_t>(sums) & 7u) != 0)
+    return DIT_ERR_MISALIGNED;
+  // out may be exactly eps_c or eps_u; any other overlap is an error.
+  const size_t bytes = static_cast<size_t>(numel) * 4;
+  if ((out != eps_c && ranges_overlap(out, bytes, eps_c, bytes)) ||
+      (out != eps_u && ranges_overlap(out, bytes, eps_u, bytes)) || ranges_overlap(sums, 16, eps_c, bytes) ||
+      ranges_overlap(sums, 16, eps_u, bytes) || ranges_overlap(sums, 16, out, bytes))
+    return DIT_ERR_INVALID_ARG;
+  int dev = 0;
+  DeviceState *st = nullptr;
+  dit_status s = select_device(stream, &dev, &st);
+  if (s != DIT_OK) return s;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(sums, 0, 2 * sizeof(double), cs) != cudaSuccess) return DIT_ERR_CUDA;
+  const long long n4 = numel / 4;
+  const int grid = stream_grid(*st, n4 > 0 ? n4 : 1);
+  ditk::cfg_combine_relmae_kernel<<<grid, ditk::kStreamThreads, 0, cs>>>(eps_c, eps_u, w, out, numel, sums);
+  return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ERR_LAUNCH;
+}
+
 dit_status dit_selftest_bounded_wait(dit_stream_t stream) {
   int dev = 0;
   DeviceState *st = nullptr;

@@ -10,6 +10,9 @@
 //   and unconditional paths of classifier-free guidance ("Accelerating
 //   Diffusion via Hybrid Data-Pipeline Parallelism Based on Conditional
 //   Guidance Scheduling", Technische Zusammenfassung 2A).
+// cfg_combine_relmae: the same combine plus, in the same pass, the two sums
+//   of the rel-MAE discrepancy between the paths that the same page (2B)
+//   switches its parallelism phases on: sum |eps_c - eps_u| and sum |eps_u|.
 //
 // Both are pure streams: each output element is written once and each input
 // element read once, 16 bytes per thread access, consecutive threads on
@@ -112,6 +115,71 @@ __global__ void __launch_bounds__(kStreamThreads)
     o.w = fmaf(w, c.w - u.w, u.w);
     st_stream(out + i, o);
   }
+}
+
+// Sums of a (diff, base) pair over the block, added to sums[0..1] in fp64.
+__device__ __forceinline__ void block_add_sums(double diff, double base, double *sums) {
+  __shared__ double red[2][kStreamThreads / 32];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    diff += __shfl_down_sync(0xffffffffu, diff, off);
+    base += __shfl_down_sync(0xffffffffu, base, off);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    red[0][warp] = diff;
+    red[1][warp] = base;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double d = 0.0, b = 0.0;
+    for (int i = 0; i < kStreamThreads / 32; ++i) {
+      d += red[0][i];
+      b += red[1][i];
+    }
+    atomicAdd(sums, d);
+    atomicAdd(sums + 1, b);
+  }
+}
+
+// One thread per float4 (grid-stride), the numel % 4 tail by the first
+// threads; per-thread sums in fp32 (one accumulator per lane of the float4),
+// fp64 from the warp level on.  sums must be zero on entry.  out may alias
+// eps_c or eps_u (each element is read and then written by the same thread).
+__global__ void __launch_bounds__(kStreamThreads)
+    cfg_combine_relmae_kernel(const float *eps_c, const float *eps_u, float w, float *out, long long numel,
+                              double *sums) {
+  const long long n4 = numel >> 2;
+  const float4 *c4 = reinterpret_cast<const float4 *>(eps_c);
+  const float4 *u4 = reinterpret_cast<const float4 *>(eps_u);
+  float4 *o4 = reinterpret_cast<float4 *>(out);
+  float4 dsum = make_float4(0.f, 0.f, 0.f, 0.f), bsum = make_float4(0.f, 0.f, 0.f, 0.f);
+  const long long tid = static_cast<long long>(blockIdx.x) * kStreamThreads + threadIdx.x;
+  const long long stride = static_cast<long long>(gridDim.x) * kStreamThreads;
+  for (long long i = tid; i < n4; i += stride) {
+    const float4 c = ld_stream(c4 + i);
+    const float4 u = ld_stream(u4 + i);
+    const float dx = c.x - u.x, dy = c.y - u.y, dz = c.z - u.z, dw = c.w - u.w;
+    st_stream(o4 + i, make_float4(fmaf(w, dx, u.x), fmaf(w, dy, u.y), fmaf(w, dz, u.z), fmaf(w, dw, u.w)));
+    dsum.x += fabsf(dx);
+    dsum.y += fabsf(dy);
+    dsum.z += fabsf(dz);
+    dsum.w += fabsf(dw);
+    bsum.x += fabsf(u.x);
+    bsum.y += fabsf(u.y);
+    bsum.z += fabsf(u.z);
+    bsum.w += fabsf(u.w);
+  }
+  double diff = (static_cast<double>(dsum.x) + dsum.y) + (static_cast<double>(dsum.z) + dsum.w);
+  double base = (static_cast<double>(bsum.x) + bsum.y) + (static_cast<double>(bsum.z) + bsum.w);
+  if (tid < numel - 4 * n4) {
+    const long long i = 4 * n4 + tid;
+    const float c = eps_c[i], u = eps_u[i];
+    out[i] = fmaf(w, c - u, u);
+    diff += fabsf(c - u);
+    base += fabsf(u);
+  }
+  block_add_sums(diff, base, sums);
 }
 
 __global__ void cfg_combine_tail_kernel(const float *eps_c, const float *eps_u, float w, float *out,

@@ -34,6 +34,7 @@ SIGNATURES = {
     "dit_attn_merge": ([_vp, _vp, ctypes.c_int, _vp, _vp, ctypes.c_longlong, ctypes.c_int, _vp],
                        ctypes.c_int),
     "cfg_combine": ([_vp, _vp, ctypes.c_float, _vp, ctypes.c_longlong, _vp], ctypes.c_int),
+    "cfg_combine_relmae": ([_vp, _vp, ctypes.c_float, _vp, ctypes.c_longlong, _vp, _vp], ctypes.c_int),
     "dit_last_device_status": ([_vp], ctypes.c_int),
     "dit_selftest_bounded_wait": ([_vp], ctypes.c_int),
     "dit_status_string": ([ctypes.c_int], ctypes.c_char_p),
@@ -161,6 +162,18 @@ def cfg_combine(eps_c, eps_u, w: float, out, stream=None) -> None:
     _check(rc, "cfg_combine")
 
 
+def cfg_combine_relmae(eps_c, eps_u, w: float, out, sums, stream=None) -> None:
+    """cfg_combine plus sums = [sum |eps_c - eps_u|, sum |eps_u|] (fp64 [2] on the
+    device); the rel-MAE discrepancy of the two guidance paths is sums[0] / sums[1]."""
+    _need(eps_c, "eps_c", torch.float32)
+    _need(eps_u, "eps_u", torch.float32, eps_c.shape)
+    _need(out, "out", torch.float32, eps_c.shape)
+    _need(sums, "sums", torch.float64, (2,))
+    rc = lib().cfg_combine_relmae(eps_c.data_ptr(), eps_u.data_ptr(), float(w), out.data_ptr(), eps_c.numel(),
+                                  sums.data_ptr(), _stream(stream))
+    _check(rc, "cfg_combine_relmae")
+
+
 def dit_last_device_status(stream=None) -> int:
     """Synchronise the stream, read and clear the device status word."""
     return int(lib().dit_last_device_status(_stream(stream)))
@@ -199,3 +212,13 @@ def combine(eps_c, eps_u, w: float, stream=None):
     out = torch.empty_like(eps_c)
     cfg_combine(eps_c, eps_u, w, out, stream)
     return out
+
+
+def combine_relmae(eps_c, eps_u, w: float, stream=None):
+    """Returns (out, rel_mae) with rel_mae = sum |eps_c - eps_u| / sum |eps_u| as a
+    Python float (reading it waits for the stream)."""
+    out = torch.empty_like(eps_c)
+    sums = torch.empty(2, dtype=torch.float64, device=eps_c.device)
+    cfg_combine_relmae(eps_c, eps_u, w, out, sums, stream)
+    d, b = sums.tolist()
+    return out, d / b

@@ -38,7 +38,7 @@ def header_functions():
 def test_header_declares_the_boundary():
     names = header_functions()
     for want in ("dit_attn_fwd", "dit_attn_fwd_partials", "dit_attn_merge", "cfg_combine",
-                 "dit_last_device_status", "dit_status_string", "dit_abi_version"):
+                 "cfg_combine_relmae", "dit_last_device_status", "dit_status_string", "dit_abi_version"):
         assert want in names
 
 
@@ -102,6 +102,18 @@ def test_cfg_rejects_bad_arguments_on_host(lib):
     assert f(A, B_, float("nan"), O, 100, None) == INVALID
     assert f(A, B_ + 4, 4.5, O, 100, None) == MISALIGNED
     assert f(A, B_, 4.5, A + 16, 100, None) == INVALID             # partial overlap
+
+
+def test_cfg_relmae_rejects_bad_arguments_on_host(lib):
+    f = lib.cfg_combine_relmae
+    S_ = 0x7F5000000000
+    assert f(A, B_, 4.5, O, 100, None, None) == INVALID             # no sums buffer
+    assert f(None, B_, 4.5, O, 100, S_, None) == INVALID
+    assert f(A, B_, 4.5, O, 0, S_, None) == INVALID
+    assert f(A, B_, float("inf"), O, 100, S_, None) == INVALID
+    assert f(A, B_, 4.5, O, 100, S_ + 4, None) == MISALIGNED        # sums not 8-byte aligned
+    assert f(A, B_, 4.5, O, 100, A + 64, None) == INVALID           # sums inside eps_c
+    assert f(A, B_, 4.5, A + 16, 100, S_, None) == INVALID          # out partly over eps_c
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU behaviour")

@@ -53,6 +53,49 @@ def test_cfg_combine_sizes_and_alias(numel):
     check_f32(dit_attn.combine(c1, u1, 0.0), eps_u.double().numpy(), "w=0")
 
 
+# ----------------------------------------------- CFG combine + rel-MAE
+def check_relmae(eps_c, eps_u, w, what):
+    ref_out, (ref_d, ref_b) = oracle.cfg_relmae(eps_c.numpy(), eps_u.numpy(), w)
+    c, u = to_dev(eps_c, eps_u)
+    out = torch.empty_like(c)
+    sums = torch.empty(2, dtype=torch.float64, device=DEV)
+    dit_attn.cfg_combine_relmae(c, u, w, out, sums)
+    check_f32(out, ref_out, f"{what} combine")
+    # the fused combine is the plain combine, bit for bit
+    assert torch.equal(out, dit_attn.combine(c, u, w)), what
+    d, b = sums.tolist()
+    assert abs(d - ref_d) <= 1e-5 * ref_d + 1e-30, (what, d, ref_d)
+    assert abs(b - ref_b) <= 1e-5 * ref_b, (what, b, ref_b)
+    assert abs(d / b - ref_d / ref_b) <= 1e-5 * (ref_d / ref_b) + 1e-30, what
+    assert_no_device_error()
+
+
+@pytest.mark.parametrize("name", ["tiny", "pixart_1024"])
+def test_cfg_relmae_workloads(name):
+    cfg = workloads.BY_NAME[name]
+    eps_c, eps_u = workloads.make_cfg(cfg.cfg_shape, workloads.seed_for(cfg, 100))
+    check_relmae(eps_c, eps_u, cfg.cfg_w, f"relmae {name}")
+
+
+@pytest.mark.parametrize("numel", [1, 3, 4, 5, 1023, 4096 + 3, 1 << 20, (1 << 24) + 7])
+def test_cfg_relmae_sizes(numel):
+    eps_c, eps_u = workloads.make_cfg((numel,), 11 + numel)
+    check_relmae(eps_c, eps_u, 4.5, f"relmae numel={numel}")
+
+
+def test_cfg_relmae_closed_forms_and_alias():
+    _, eps_u = workloads.make_cfg((4096 + 1,), 5)
+    for c, want in ((eps_u.clone(), 0.0), (2.0 * eps_u, 1.0), (-eps_u, 2.0)):
+        cd, ud = to_dev(c, eps_u)
+        out, rel = dit_attn.combine_relmae(cd, ud, 4.5)
+        assert abs(rel - want) <= 1e-6, (want, rel)
+    c, u = to_dev(*workloads.make_cfg((1000,), 6))
+    ref = dit_attn.combine(c, u, 4.5)
+    sums = torch.empty(2, dtype=torch.float64, device=DEV)
+    dit_attn.cfg_combine_relmae(c, u, 4.5, c, sums)       # in place over eps_c
+    assert torch.equal(c, ref)
+
+
 # ------------------------------------------------------------- LSE merge
 @pytest.mark.parametrize("n,rows,D", [(1, 100, 64), (2, 777, 72), (5, 300, 128), (16, 4096, 64),
                                       (3, 50, 7), (16, 333, 1)])
