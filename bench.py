@@ -73,13 +73,19 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash():
+# The sources the attention kernel is compiled from: its device code and the
+# launch (tensor maps, grid) in the C ABI file.
+ATTN_SOURCES = ("attn_fwd.cuh", "ptx.cuh", "dit_attn.cu")
+
+
+def kernel_source_hash(names=ATTN_SOURCES):
+    """Short hash of the attention kernel's sources; a recorded ncu traffic
+    figure is used only while this hash matches the one it was taken on."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sequence_attention_attn_b300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in sorted(names):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
