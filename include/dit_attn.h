@@ -94,6 +94,57 @@ dit_status dit_attn_fwd_partials(const void *q, const void *k, const void *v,
                                  dit_stream_t stream);
 
 /*
+ * dit_attn_fwd_range -- attention of every query over one key range
+ * [j0, j1): the computation a device of a ring / Torus sequence-parallel
+ * split performs on the piece of K/V it holds ("SwiftFusion ...", ideas 1 and
+ * 2: each piece is computed as it arrives and its partial result folded in
+ * later).  Per (b, h) and query row i, with s_ij = q_i . k_j / sqrt(D):
+ *     LSE_i = ln sum_{j0 <= j < j1} exp(s_ij),
+ *     out_i = sum_{j0 <= j < j1} exp(s_ij - LSE_i) v_j.
+ *
+ *   q, k, v      bf16 [B, H, S, D] as for dit_attn_fwd (only key rows
+ *                [j0, j1) of k and v are read, plus the rest of the last
+ *                128-key tile, whose weights are masked to 0 but which must
+ *                hold finite values).
+ *   out          fp32 [B * H * S, D], 16-byte aligned.
+ *   lse          fp32 [B * H * S], 16-byte aligned.
+ *   j0, j1       0 <= j0 < j1 <= S (else DIT_ERR_INVALID_ARG).
+ */
+dit_status dit_attn_fwd_range(const void *q, const void *k, const void *v,
+                              float *out, float *lse, int B, int H, int S,
+                              int D, int j0, int j1, dit_stream_t stream);
+
+/*
+ * dit_attn_fwd_torus -- Torus-style chunked attention on one GPU: the K/V
+ * rows of chunk c (the balanced partition of dit_attn_fwd) are copied from
+ * k_src / v_src into k / v on copy_stream, one event per chunk, and chunk c
+ * is computed on stream (dit_attn_fwd_range into partials[c], lses[c]) as
+ * soon as its rows -- and those of any later chunk its last tile reaches --
+ * have arrived, while later chunks are still being copied; then
+ * dit_attn_merge combines the partials into out / lse_out.  Source:
+ * "SwiftFusion ..." (idea 2: Torus attention splits a received block into
+ * pieces and computes piece i while piece i + 1 arrives); on one GPU the
+ * arrival is a copy and the overlap is between the copy engine and the SMs.
+ *
+ *   q            bf16 [B, H, S, D] device.
+ *   k_src, v_src bf16 [B, H, S, D]: pinned host or device memory.
+ *   k, v         bf16 [B, H, S, D] device buffers the copies land in.
+ *   partials     fp32 [n_kv_chunks, B * H * S, D]; lses fp32 [n_kv_chunks, B * H * S].
+ *   out          fp32 [B * H * S, D]; lse_out fp32 [B * H * S] or NULL.
+ *   n_kv_chunks  1 <= n_kv_chunks <= min(S, 64).
+ *   copy_stream  the stream of the copies (NULL or == stream: no overlap).
+ * The copies wait for the work queued on `stream` before this call; the
+ * result is complete when `stream` reaches the end of this call's work.
+ * Uses per-device events created on the first call (no device memory).
+ */
+dit_status dit_attn_fwd_torus(const void *q, const void *k_src,
+                              const void *v_src, void *k, void *v,
+                              float *partials, float *lses, float *out,
+                              float *lse_out, int B, int H, int S, int D,
+                              int n_kv_chunks, dit_stream_t stream,
+                              dit_stream_t copy_stream);
+
+/*
  * dit_attn_merge -- log-sum-exp merge of n partial attention results, the
  * recombination step of ring / Torus sequence-parallel attention
  * ("SwiftFusion ...", ideas 1 and 2).  For each row r:

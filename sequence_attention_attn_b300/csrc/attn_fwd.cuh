@@ -105,6 +105,7 @@ struct AttnParams {
   int n_chunks;
   int num_pairs;       // ceil(ceil(S / 128) / 2)
   int tiles_total;     // merged mode: number of key tiles over all chunks
+  int key_j0, key_j1;  // partials mode with key_j1 > 0: one key range, written to slot 0
   float scale_log2;    // log2(e) / sqrt(D)
 };
 
@@ -118,6 +119,15 @@ struct KvIter {
     j0 = static_cast<int>((static_cast<long long>(c) * S) / n);
     j1 = static_cast<int>((static_cast<long long>(c + 1) * S) / n);
     t0 = j0;
+  }
+  // A single explicit key range [j0_, j1_) (one chunk).
+  __device__ __forceinline__ void start_range(int j0_, int j1_) {
+    S = j1_;
+    n = 1;
+    c = 0;
+    j0 = j0_;
+    j1 = j1_;
+    t0 = j0_;
   }
   __device__ __forceinline__ int valid() const { return min(kBlockN, j1 - t0); }
   __device__ __forceinline__ bool chunk_start() const { return t0 == j0; }
@@ -251,8 +261,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int bc = u / per_bh_chunk;
     chunk_first = bc % p.n_chunks;
     bh = bc / p.n_chunks;
-    const long long j0 = (static_cast<long long>(chunk_first) * p.S) / p.n_chunks;
-    const long long j1 = (static_cast<long long>(chunk_first + 1) * p.S) / p.n_chunks;
+    const long long j0 = p.key_j1 > 0 ? p.key_j0 : (static_cast<long long>(chunk_first) * p.S) / p.n_chunks;
+    const long long j1 = p.key_j1 > 0 ? p.key_j1 : (static_cast<long long>(chunk_first + 1) * p.S) / p.n_chunks;
     tiles = static_cast<int>((j1 - j0 + kBlockN - 1) / kBlockN);
   } else {
     pair = blockIdx.x % p.num_pairs;
@@ -329,7 +339,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           tma_load_3d(dst + kSwzBytes, &tm_q_tail, q_full(t), 64, q_row0 + t * kBlockM, bh, pol_q);
       }
       KvIter kv;
-      kv.start(p.S, p.n_chunks, chunk_first);
+      if (kPartials && p.key_j1 > 0) kv.start_range(p.key_j0, p.key_j1);
+      else kv.start(p.S, p.n_chunks, chunk_first);
       int k_last[NS], v_last[NS];  // last use issued on each stage, -1 if none
 #pragma unroll
       for (int s = 0; s < NS; ++s) k_last[s] = v_last[s] = -1;
@@ -428,7 +439,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       float l = 0.0f;          // row sum of the current chunk
       float l_run = -INFINITY; // merged log2-LSE of finished chunks
       KvIter kv;
-      kv.start(p.S, p.n_chunks, chunk_first);
+      if (kPartials && p.key_j1 > 0) kv.start_range(p.key_j0, p.key_j1);
+      else kv.start(p.S, p.n_chunks, chunk_first);
       bool ok = true;
       for (int it = 0; it < tiles; ++it) {
         if (!(ok = mbar_wait_warp(s_full(t), it & 1))) break;

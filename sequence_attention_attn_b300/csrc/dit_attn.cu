@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -31,14 +32,21 @@ bool ranges_overlap(const void *a, size_t a_bytes, const void *b, size_t b_bytes
   return a0 < b0 + b_bytes && b0 < a0 + a_bytes;
 }
 
+constexpr int kMaxTorusChunks = 64;
+
 struct DeviceState {
   bool probed = false;
   bool supported = false;
   int sm_count = 0;
+  // Events of the Torus pipeline (created on first use, reused by every call).
+  cudaEvent_t torus_events[kMaxTorusChunks + 1] = {};
+  bool torus_events_ready = false;
   bool attr_set[3][2] = {};  // per head-dim instantiation x partials
 };
 
 std::mutex g_mu;
+// Serialises dit_attn_fwd_torus calls: they share one event pool per device.
+std::mutex g_torus_mu;
 DeviceState g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -148,9 +156,12 @@ dit_status launch_attn(DeviceState &st, int didx, const void *q, const void *k, 
   return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ERR_LAUNCH;
 }
 
+// key_j1 > 0 (partials mode only): one key range [key_j0, key_j1), written
+// to the first partial slot.
 template <bool kPartials>
 dit_status attn_dispatch(const void *q, const void *k, const void *v, void *out, float *lse, float *partials,
-                         float *part_lse, int B, int H, int S, int D, int n, dit_stream_t stream) {
+                         float *part_lse, int B, int H, int S, int D, int n, dit_stream_t stream, int key_j0 = 0,
+                         int key_j1 = 0) {
   const long long BH = static_cast<long long>(B) * H;
   const int tiles_q = (S + ditk::kBlockM - 1) / ditk::kBlockM;
   const int num_pairs = (tiles_q + 1) / 2;
@@ -180,6 +191,8 @@ dit_status attn_dispatch(const void *q, const void *k, const void *v, void *out,
   prm.n_chunks = n;
   prm.num_pairs = num_pairs;
   prm.tiles_total = static_cast<int>(tiles_total);
+  prm.key_j0 = key_j0;
+  prm.key_j1 = key_j1;
   prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   switch (D) {
@@ -262,6 +275,106 @@ dit_status dit_attn_fwd_partials(const void *q, const void *k, const void *v, fl
       ranges_overlap(lses, l_bytes, partials, p_bytes))
     return DIT_ERR_INVALID_ARG;
   return attn_dispatch<true>(q, k, v, nullptr, nullptr, partials, lses, B, H, S, D, n_kv_chunks, stream);
+}
+
+dit_status dit_attn_fwd_range(const void *q, const void *k, const void *v, float *out, float *lse, int B, int H,
+                              int S, int D, int j0, int j1, dit_stream_t stream) {
+  dit_status s = check_attn_args(q, k, v, B, H, S, D, 1);
+  if (s != DIT_OK) return s;
+  if (out == nullptr || lse == nullptr) return DIT_ERR_INVALID_ARG;
+  if (j0 < 0 || j1 > S || j0 >= j1) return DIT_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(lse)) return DIT_ERR_MISALIGNED;
+  const size_t in_bytes = static_cast<size_t>(B) * H * S * D * 2;
+  const size_t o_bytes = static_cast<size_t>(B) * H * S * D * 4;
+  const size_t l_bytes = static_cast<size_t>(B) * H * S * 4;
+  if (ranges_overlap(out, o_bytes, q, in_bytes) || ranges_overlap(out, o_bytes, k, in_bytes) ||
+      ranges_overlap(out, o_bytes, v, in_bytes) || ranges_overlap(lse, l_bytes, q, in_bytes) ||
+      ranges_overlap(lse, l_bytes, k, in_bytes) || ranges_overlap(lse, l_bytes, v, in_bytes) ||
+      ranges_overlap(lse, l_bytes, out, o_bytes))
+    return DIT_ERR_INVALID_ARG;
+  return attn_dispatch<true>(q, k, v, nullptr, nullptr, out, lse, B, H, S, D, 1, stream, j0, j1);
+}
+
+dit_status dit_attn_fwd_torus(const void *q, const void *k_src, const void *v_src, void *k, void *v,
+                              float *partials, float *lses, float *out, float *lse_out, int B, int H, int S, int D,
+                              int n_kv_chunks, dit_stream_t stream, dit_stream_t copy_stream) {
+  const int n = n_kv_chunks;
+  dit_status s = check_attn_args(q, k, v, B, H, S, D, n);
+  if (s != DIT_OK) return s;
+  if (n > kMaxTorusChunks) return DIT_ERR_INVALID_ARG;
+  if (k_src == nullptr || v_src == nullptr || partials == nullptr || lses == nullptr || out == nullptr)
+    return DIT_ERR_INVALID_ARG;
+  if (!aligned16(partials) || !aligned16(lses) || !aligned16(out) || (lse_out != nullptr && !aligned16(lse_out)))
+    return DIT_ERR_MISALIGNED;
+  const long long BH = static_cast<long long>(B) * H;
+  const long long rows = BH * S;
+  const size_t kv_bytes = static_cast<size_t>(rows) * D * 2;
+  const size_t p_bytes = static_cast<size_t>(n) * rows * D * 4, l_bytes = static_cast<size_t>(n) * rows * 4;
+  const size_t o_bytes = static_cast<size_t>(rows) * D * 4;
+  const void *dev_bufs[] = {q, k, v};
+  for (const void *b : dev_bufs) {
+    if (ranges_overlap(partials, p_bytes, b, kv_bytes) || ranges_overlap(lses, l_bytes, b, kv_bytes) ||
+        ranges_overlap(out, o_bytes, b, kv_bytes))
+      return DIT_ERR_INVALID_ARG;
+  }
+  if (ranges_overlap(k, kv_bytes, v, kv_bytes) || ranges_overlap(k, kv_bytes, q, kv_bytes) ||
+      ranges_overlap(v, kv_bytes, q, kv_bytes) || ranges_overlap(k_src, kv_bytes, k, kv_bytes) ||
+      ranges_overlap(v_src, kv_bytes, v, kv_bytes) || ranges_overlap(lses, l_bytes, partials, p_bytes))
+    return DIT_ERR_INVALID_ARG;
+  int dev = 0;
+  DeviceState *st = nullptr;
+  if ((s = select_device(stream, &dev, &st)) != DIT_OK) return s;
+  std::lock_guard<std::mutex> torus_lock(g_torus_mu);
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!st->torus_events_ready) {
+      for (int i = 0; i <= kMaxTorusChunks; ++i)
+        if (cudaEventCreateWithFlags(&st->torus_events[i], cudaEventDisableTiming) != cudaSuccess)
+          return DIT_ERR_CUDA;
+      st->torus_events_ready = true;
+    }
+  }
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaStream_t xs = copy_stream != nullptr ? reinterpret_cast<cudaStream_t>(copy_stream) : cs;
+  cudaEvent_t *ev = st->torus_events;
+  // The copies may only overwrite k and v once the work queued before this
+  // call on the compute stream (which may still read them) is done.
+  if (xs != cs) {
+    if (cudaEventRecord(ev[kMaxTorusChunks], cs) != cudaSuccess) return DIT_ERR_CUDA;
+    if (cudaStreamWaitEvent(xs, ev[kMaxTorusChunks], 0) != cudaSuccess) return DIT_ERR_CUDA;
+  }
+  const size_t pitch = static_cast<size_t>(S) * D * 2;
+  auto bound = [&](int c) { return static_cast<int>((static_cast<long long>(c) * S) / n); };
+  // Chunk c's key rows of every (batch, head): one strided copy per tensor.
+  for (int c = 0; c < n; ++c) {
+    const size_t off = static_cast<size_t>(bound(c)) * D * 2, width = static_cast<size_t>(bound(c + 1) - bound(c)) * D * 2;
+    if (cudaMemcpy2DAsync(static_cast<char *>(k) + off, pitch, static_cast<const char *>(k_src) + off, pitch, width,
+                          static_cast<size_t>(BH), cudaMemcpyDefault, xs) != cudaSuccess ||
+        cudaMemcpy2DAsync(static_cast<char *>(v) + off, pitch, static_cast<const char *>(v_src) + off, pitch, width,
+                          static_cast<size_t>(BH), cudaMemcpyDefault, xs) != cudaSuccess)
+      return DIT_ERR_CUDA;
+    if (cudaEventRecord(ev[c], xs) != cudaSuccess) return DIT_ERR_CUDA;
+  }
+  // Chunk c is computed once its rows have arrived.  Its last 128-key tile
+  // also reads (and masks) rows past the chunk end, which must hold finished
+  // data (a masked weight of 0 times an unfinished NaN is NaN), so the wait
+  // covers every chunk that tile reaches.
+  const long long tile = ditk::kBlockN;
+  int waited = -1;
+  for (int c = 0; c < n; ++c) {
+    const long long j0 = bound(c), j1 = bound(c + 1);
+    const long long reach = std::min<long long>(S, j0 + (j1 - j0 + tile - 1) / tile * tile) - 1;
+    int last = c;
+    while (last + 1 < n && bound(last + 1) <= reach) ++last;
+    for (int w = waited + 1; w <= last; ++w)
+      if (cudaStreamWaitEvent(cs, ev[w], 0) != cudaSuccess) return DIT_ERR_CUDA;
+    waited = std::max(waited, last);
+    s = attn_dispatch<true>(q, k, v, nullptr, nullptr, partials + static_cast<size_t>(c) * rows * D,
+                            lses + static_cast<size_t>(c) * rows, B, H, S, D, 1, stream, static_cast<int>(j0),
+                            static_cast<int>(j1));
+    if (s != DIT_OK) return s;
+  }
+  return dit_attn_merge(partials, lses, n, out, lse_out, rows, D, stream);
 }
 
 dit_status dit_attn_merge(const float *partials, const float *lses, int n, float *out, float *lse_out,

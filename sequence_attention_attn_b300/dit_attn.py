@@ -33,6 +33,10 @@ SIGNATURES = {
                                ctypes.c_int, ctypes.c_int, _vp], ctypes.c_int),
     "dit_attn_merge": ([_vp, _vp, ctypes.c_int, _vp, _vp, ctypes.c_longlong, ctypes.c_int, _vp],
                        ctypes.c_int),
+    "dit_attn_fwd_range": ([_vp, _vp, _vp, _vp, _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                            ctypes.c_int, ctypes.c_int, _vp], ctypes.c_int),
+    "dit_attn_fwd_torus": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, ctypes.c_int,
+                            ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _vp], ctypes.c_int),
     "cfg_combine": ([_vp, _vp, ctypes.c_float, _vp, ctypes.c_longlong, _vp], ctypes.c_int),
     "cfg_combine_relmae": ([_vp, _vp, ctypes.c_float, _vp, ctypes.c_longlong, _vp, _vp], ctypes.c_int),
     "dit_last_device_status": ([_vp], ctypes.c_int),
@@ -162,6 +166,54 @@ def cfg_combine(eps_c, eps_u, w: float, out, stream=None) -> None:
     _check(rc, "cfg_combine")
 
 
+def dit_attn_fwd_range(q, k, v, out, lse, j0: int, j1: int, stream=None) -> None:
+    """Attention over keys [j0, j1): out fp32 [B*H*S, D], lse fp32 [B*H*S]."""
+    _need(q, "q", torch.bfloat16)
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, S, D]")
+    B, H, S, D = q.shape
+    _need(k, "k", torch.bfloat16, q.shape)
+    _need(v, "v", torch.bfloat16, q.shape)
+    _need(out, "out", torch.float32, (B * H * S, D))
+    _need(lse, "lse", torch.float32, (B * H * S,))
+    rc = lib().dit_attn_fwd_range(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                  B, H, S, D, int(j0), int(j1), _stream(stream))
+    _check(rc, "dit_attn_fwd_range")
+
+
+def dit_attn_fwd_torus(q, k_src, v_src, k, v, partials, lses, out, lse_out, n_kv_chunks: int, stream=None,
+                       copy_stream=None) -> None:
+    """Torus-style chunked attention: K/V chunks copied from k_src / v_src (pinned
+    host or device tensors) into k / v on copy_stream while earlier chunks are
+    computed on stream; partials fp32 [n, B*H*S, D], lses fp32 [n, B*H*S], out fp32
+    [B*H*S, D], lse_out fp32 [B*H*S] or None."""
+    _need(q, "q", torch.bfloat16)
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, S, D]")
+    B, H, S, D = q.shape
+    n = int(n_kv_chunks)
+    rows = B * H * S
+    for t, name in ((k_src, "k_src"), (v_src, "v_src")):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or tuple(t.shape) != tuple(q.shape) \
+                or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 tensor shaped like q")
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    _need(k, "k", torch.bfloat16, q.shape)
+    _need(v, "v", torch.bfloat16, q.shape)
+    _need(partials, "partials", torch.float32, (n, rows, D))
+    _need(lses, "lses", torch.float32, (n, rows))
+    _need(out, "out", torch.float32, (rows, D))
+    if lse_out is not None:
+        _need(lse_out, "lse_out", torch.float32, (rows,))
+    cs = None if copy_stream is None else _stream(copy_stream)
+    rc = lib().dit_attn_fwd_torus(q.data_ptr(), k_src.data_ptr(), v_src.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                  partials.data_ptr(), lses.data_ptr(), out.data_ptr(),
+                                  None if lse_out is None else lse_out.data_ptr(), B, H, S, D, n,
+                                  _stream(stream), cs)
+    _check(rc, "dit_attn_fwd_torus")
+
+
 def cfg_combine_relmae(eps_c, eps_u, w: float, out, sums, stream=None) -> None:
     """cfg_combine plus sums = [sum |eps_c - eps_u|, sum |eps_u|] (fp64 [2] on the
     device); the rel-MAE discrepancy of the two guidance paths is sums[0] / sums[1]."""
@@ -212,6 +264,35 @@ def combine(eps_c, eps_u, w: float, stream=None):
     out = torch.empty_like(eps_c)
     cfg_combine(eps_c, eps_u, w, out, stream)
     return out
+
+
+def attention_range(q, k, v, j0: int, j1: int, stream=None):
+    B, H, S, D = q.shape
+    out = torch.empty((B * H * S, D), dtype=torch.float32, device=q.device)
+    lse = torch.empty((B * H * S,), dtype=torch.float32, device=q.device)
+    dit_attn_fwd_range(q, k, v, out, lse, j0, j1, stream)
+    return out, lse
+
+
+def attention_torus(q, k_src, v_src, n_kv_chunks: int, stream=None, copy_stream=None):
+    """Returns (out fp32 [B*H*S, D], lse fp32 [B*H*S]); allocates the device K/V
+    landing buffers and the partials with torch."""
+    B, H, S, D = q.shape
+    rows = B * H * S
+    k = torch.empty_like(q)
+    v = torch.empty_like(q)
+    partials = torch.empty((n_kv_chunks, rows, D), dtype=torch.float32, device=q.device)
+    lses = torch.empty((n_kv_chunks, rows), dtype=torch.float32, device=q.device)
+    out = torch.empty((rows, D), dtype=torch.float32, device=q.device)
+    lse = torch.empty((rows,), dtype=torch.float32, device=q.device)
+    dit_attn_fwd_torus(q, k_src, v_src, k, v, partials, lses, out, lse, n_kv_chunks, stream, copy_stream)
+    # The buffers were allocated on torch's current stream; keep the caching
+    # allocator from handing them out again before the other streams finish.
+    for s_ in (stream, copy_stream):
+        if isinstance(s_, torch.cuda.Stream):
+            for t in (k, v, partials, lses, out, lse):
+                t.record_stream(s_)
+    return out, lse
 
 
 def combine_relmae(eps_c, eps_u, w: float, stream=None):

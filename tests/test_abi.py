@@ -38,7 +38,7 @@ def header_functions():
 def test_header_declares_the_boundary():
     names = header_functions()
     for want in ("dit_attn_fwd", "dit_attn_fwd_partials", "dit_attn_merge", "cfg_combine",
-                 "cfg_combine_relmae", "dit_last_device_status", "dit_status_string", "dit_abi_version"):
+                 "cfg_combine_relmae", "dit_attn_fwd_range", "dit_attn_fwd_torus", "dit_last_device_status", "dit_status_string", "dit_abi_version"):
         assert want in names
 
 
@@ -130,3 +130,40 @@ def test_python_binding_refuses_cpu_tensors(lib):
         dit_attn.attention(q, q, q)
     with pytest.raises(ValueError, match="CUDA"):
         dit_attn.combine(torch.zeros(4), torch.zeros(4), 1.0)
+
+
+def test_range_rejects_bad_arguments_on_host(lib):
+    f = lib.dit_attn_fwd_range
+    assert f(A, B_, C, O, L, 1, 2, 256, 64, -1, 10, None) == INVALID
+    assert f(A, B_, C, O, L, 1, 2, 256, 64, 0, 257, None) == INVALID          # j1 past S
+    assert f(A, B_, C, O, L, 1, 2, 256, 64, 10, 10, None) == INVALID          # empty range
+    assert f(A, B_, C, O, L, 1, 2, 256, 64, 20, 10, None) == INVALID
+    assert f(A, B_, C, None, L, 1, 2, 256, 64, 0, 10, None) == INVALID
+    assert f(A, B_, C, O, None, 1, 2, 256, 64, 0, 10, None) == INVALID
+    assert f(A, B_, C, O + 4, L, 1, 2, 256, 64, 0, 10, None) == MISALIGNED
+    assert f(A, B_, C, O, L, 1, 2, 256, 65, 0, 10, None) == SHAPE
+    assert f(A, B_, C, B_ + 256, L, 1, 2, 256, 64, 0, 10, None) == INVALID    # out overlaps k
+    assert f(A, B_, C, O, O + 64, 1, 2, 256, 64, 0, 10, None) == INVALID      # lse overlaps out
+
+
+def test_torus_rejects_bad_arguments_on_host(lib):
+    f = lib.dit_attn_fwd_torus
+    KS, VS, K, V, P = 0x7F5000000000, 0x7F6000000000, 0x7F7000000000, 0x7F8000000000, 0x7F9000000000
+
+    def call(q=A, ks=KS, vs=VS, k=K, v=V, p=P, ls=L, out=O, lo=None, S=256, D=64, n=4):
+        return f(q, ks, vs, k, v, p, ls, out, lo, 1, 2, S, D, n, None, None)
+
+    assert call(n=0) == INVALID
+    assert call(n=65) == INVALID                  # more chunks than the event pool holds
+    assert call(n=257) == INVALID                 # more chunks than keys
+    assert call(ks=None) == INVALID
+    assert call(vs=None) == INVALID
+    assert call(p=None) == INVALID
+    assert call(out=None) == INVALID
+    assert call(D=96) == SHAPE
+    assert call(p=P + 8) == MISALIGNED
+    assert call(lo=L + 0x1000000 + 4) == MISALIGNED
+    assert call(k=V) == INVALID                   # k and v the same buffer
+    assert call(p=A) == INVALID                   # partials over q
+    assert call(ks=K) == INVALID                  # source is the landing buffer
+    assert call(ls=P + 64) == INVALID             # lses inside partials
