@@ -156,9 +156,7 @@ __global__ void __launch_bounds__(kStreamThreads)
   float4 dsum = make_float4(0.f, 0.f, 0.f, 0.f), bsum = make_float4(0.f, 0.f, 0.f, 0.f);
   const long long tid = static_cast<long long>(blockIdx.x) * kStreamThreads + threadIdx.x;
   const long long stride = static_cast<long long>(gridDim.x) * kStreamThreads;
-  for (long long i = tid; i < n4; i += stride) {
-    const float4 c = ld_stream(c4 + i);
-    const float4 u = ld_stream(u4 + i);
+  auto step = [&](const float4 &c, const float4 &u, long long i) {
     const float dx = c.x - u.x, dy = c.y - u.y, dz = c.z - u.z, dw = c.w - u.w;
     st_stream(o4 + i, make_float4(fmaf(w, dx, u.x), fmaf(w, dy, u.y), fmaf(w, dz, u.z), fmaf(w, dw, u.w)));
     dsum.x += fabsf(dx);
@@ -169,7 +167,17 @@ __global__ void __launch_bounds__(kStreamThreads)
     bsum.y += fabsf(u.y);
     bsum.z += fabsf(u.z);
     bsum.w += fabsf(u.w);
+  };
+  // Two grid-stride elements per trip, both pairs of loads issued before
+  // either is used: the running sums would otherwise keep one pair in flight.
+  long long i = tid;
+  for (; i + stride < n4; i += 2 * stride) {
+    const float4 c0 = ld_stream(c4 + i), u0 = ld_stream(u4 + i);
+    const float4 c1 = ld_stream(c4 + i + stride), u1 = ld_stream(u4 + i + stride);
+    step(c0, u0, i);
+    step(c1, u1, i + stride);
   }
+  if (i < n4) step(ld_stream(c4 + i), ld_stream(u4 + i), i);
   double diff = (static_cast<double>(dsum.x) + dsum.y) + (static_cast<double>(dsum.z) + dsum.w);
   double base = (static_cast<double>(bsum.x) + bsum.y) + (static_cast<double>(bsum.z) + bsum.w);
   if (tid < numel - 4 * n4) {
