@@ -11,16 +11,26 @@
 // Design (one CTA = one (batch*head, pair of 128-row query tiles)):
 //   warp 0      TMA producer: Q tiles once, then K and V tiles (128 keys each)
 //               through NS-stage shared-memory rings.
-//   warp 1      allocates 512 TMEM columns; one lane issues every tcgen05.mma:
-//               S_t = Q_t K^T (SS form, fp32 in TMEM) and O_t += P_t V
-//               (TS form: P read from TMEM, V from shared memory).
+//   warp 1      allocates 512 TMEM columns and issues every tcgen05
+//               instruction: S_t = Q_t K^T (SS form, fp32 in TMEM) and
+//               O_t += P_t V (TS form: P read from TMEM, V from shared memory).
+//               The whole warp runs the issue loop with warp-uniform operands
+//               and one elected lane executes each MMA and commit; issuing
+//               from a single lane inside a divergent branch cost about twice
+//               as many cycles per MMA.
 //   warps 2-5   softmax for query tile 0, warps 6-9 for query tile 1.  Each
 //               thread owns one query row (one TMEM lane): it loads its S row,
 //               takes the row max, rescales its O row in TMEM when the
 //               reference max has to move, writes P = 2^(S*scale - m) as bf16
-//               over the first 64 columns of its S row, and keeps the row sum.
-// The two softmax groups ping-pong: while one group works on its S tile the
-// tensor core runs the other tile's PV and QK^T.
+//               and keeps the row sum.
+// TMEM columns: S_t at 128 t.  D = 64: O_t at 256 + 64 t and P_t at
+// 384 + 64 t, so S_t of the next key tile is computed as soon as the softmax
+// has loaded S_t into registers (QK^T runs while the softmax works) and only
+// the PV that reads P_t has to wait for it.  D = 72, 128: no room for P on
+// its own; O_t at 256 + 128 t and P_t over the first 64 columns of S_t, so
+// QK^T of the next tile follows the PV of this one.
+// The two softmax groups ping-pong: while one group works on its tile the
+// tensor core runs the other tile's MMAs.
 //
 // Online softmax in base 2: x = S * log2(e) / sqrt(D).  The reference max m
 // only moves when a tile's max exceeds it by more than kRescaleThreshold, so
@@ -87,7 +97,7 @@ struct AttnLayout {
   static constexpr int kKOff = 2 * kTileBytes;
   static constexpr int kVOff = kKOff + C::kStages * kTileBytes;
   static constexpr int kBarOff = kVOff + C::kStages * kVTileBytes;
-  static constexpr int kNumBars = 2 + 4 * C::kStages + 7;
+  static constexpr int kNumBars = 2 + 4 * C::kStages + 11;
   static constexpr int kTmemSlotOff = kBarOff + 8 * kNumBars;
   static constexpr int kBytes = kTmemSlotOff + 16;
   static constexpr int kSmemLaunch = kBytes + 1024;  // slack for 1024-byte alignment
@@ -149,41 +159,39 @@ __device__ __forceinline__ float logaddexp2(float a, float b) {
 }
 
 // ------------------------------------------------------------ MMA issue
+// Shared-memory descriptors as (low, high) words: the high word is fixed per
+// operand layout, and stepping along K or to another stage is one add on the
+// low word.
+constexpr uint32_t kHi128 = desc_hi(1024, kSwizzle128B);
+constexpr uint32_t kHi32 = desc_hi(256, kSwizzle32B);
+
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t tS, uint32_t q_smem, uint32_t k_smem) {
+__device__ __forceinline__ void issue_qk(uint32_t tS, uint32_t q_lo, uint32_t k_lo) {
   constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, kBlockN, false);
 #pragma unroll
-  for (int ks = 0; ks < 4; ++ks) {
-    const uint64_t a = smem_desc(q_smem + ks * 32, 16, 1024, kSwizzle128B);
-    const uint64_t b = smem_desc(k_smem + ks * 32, 16, 1024, kSwizzle128B);
-    umma_ss(tS, a, b, idesc, ks > 0 ? 1u : 0u);
-  }
+  for (int ks = 0; ks < 4; ++ks)
+    umma_ss_e(tS, q_lo + 2 * ks, kHi128, k_lo + 2 * ks, kHi128, idesc, ks > 0 ? 1u : 0u);
+  constexpr uint32_t kBlk = kSwzBytes >> 4;
   if constexpr (D == 128) {
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      const uint64_t a = smem_desc(q_smem + kSwzBytes + ks * 32, 16, 1024, kSwizzle128B);
-      const uint64_t b = smem_desc(k_smem + kSwzBytes + ks * 32, 16, 1024, kSwizzle128B);
-      umma_ss(tS, a, b, idesc, 1u);
-    }
+    for (int ks = 0; ks < 4; ++ks)
+      umma_ss_e(tS, q_lo + kBlk + 2 * ks, kHi128, k_lo + kBlk + 2 * ks, kHi128, idesc, 1u);
   } else if constexpr (D == 72) {
-    const uint64_t a = smem_desc(q_smem + kSwzBytes, 16, 256, kSwizzle32B);
-    const uint64_t b = smem_desc(k_smem + kSwzBytes, 16, 256, kSwizzle32B);
-    umma_ss(tS, a, b, idesc, 1u);
+    umma_ss_e(tS, q_lo + kBlk, kHi32, k_lo + kBlk, kHi32, idesc, 1u);
   }
 }
 
 // O (+)= P V: P is bf16 in TMEM (8 columns per 16 keys), V is MN-major in
-// shared memory (rows = keys, 128 bytes per row per 64-column block).
+// shared memory (rows = keys, 128 bytes per row per 64-column block).  One
+// MMA of N = Dpad per 16 keys; v_lo carries the leading byte offset from one
+// 64-column block of V to the next.
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_smem, bool accumulate) {
-  // One MMA of N = Dpad per 16 keys; the leading byte offset steps from one
-  // 64-column block of V to the next.
+__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_lo, bool accumulate) {
   constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, AttnCfg<D>::kDpad, true);
 #pragma unroll
   for (int ks = 0; ks < kBlockN / 16; ++ks) {
     const uint32_t acc = (accumulate || ks > 0) ? 1u : 0u;
-    const uint64_t b = smem_desc(v_smem + ks * 2048, kSwzBytes, 1024, kSwizzle128B);
-    umma_ts(tO, tP + ks * 8, b, idesc, acc);
+    umma_ts_e(tO, tP + ks * 8, v_lo + ks * (2048 >> 4), kHi128, idesc, acc);
   }
 }
 
@@ -287,6 +295,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   auto p_full = [&](int t) { return bars + 8u * (4 + 4 * NS + t); };
   auto o_full = [&](int t) { return bars + 8u * (6 + 4 * NS + t); };
   const uint32_t mma_done = bars + 8u * (8 + 4 * NS);
+  auto s_free = [&](int t) { return bars + 8u * (9 + 4 * NS + t); };
+  auto o_upd = [&](int t) { return bars + 8u * (11 + 4 * NS + t); };
+  // s_free(t): the softmax group has loaded S_t (D = 64 only); o_upd(t): the
+  // PV of tile t has completed, so P_t and O_t are free (D = 64 only).
+  constexpr bool kSplitP = (D == 64);
+  constexpr uint32_t kOStride = kSplitP ? 64u : 128u;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kTmemSlotOff);
 
   if (threadIdx.x == 0) {
@@ -304,6 +318,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(o_full(t), 1);
     }
     mbar_init(mma_done, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(s_free(t), kBlockM);
+      mbar_init(o_upd(t), 1);
+    }
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -374,55 +392,89 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issue
-    if (lane == 0) {
+    // The whole warp runs the loop; one elected lane issues each instruction.
+    {
       const uint32_t tS0 = tmem_base, tS1 = tmem_base + 128;
-      const uint32_t tO0 = tmem_base + 256, tO1 = tmem_base + 384;
-      bool ok = mbar_wait(q_full(0), 0) && (!has1 || mbar_wait(q_full(1), 0));
+      const uint32_t tO0 = tmem_base + 256, tO1 = tmem_base + 256 + kOStride;
+      const uint32_t tP0 = kSplitP ? tmem_base + 384 : tS0, tP1 = kSplitP ? tmem_base + 448 : tS1;
+      const uint32_t q_lo0 = desc_lo(sQ0, 16), k_lo0 = desc_lo(sK0, 16), v_lo0 = desc_lo(sV0, kSwzBytes);
+      bool ok = mbar_wait_warp(q_full(0), 0) && (!has1 || mbar_wait_warp(q_full(1), 0));
       tc_fence_after();
       for (int it = 0; ok && it < tiles; ++it) {
         const int s = it % NS, u = it / NS;
-        if (!(ok = mbar_wait(k_full(s), u & 1))) break;
+        if (!(ok = mbar_wait_warp(k_full(s), u & 1))) break;
         tc_fence_after();
-        const uint32_t ks = sK0 + s * kTileBytes;
+        const uint32_t ks = k_lo0 + s * (kTileBytes >> 4);
         const int ps = (it + NS - 1) % NS;
-        const uint32_t vs = sV0 + ps * kVTileBytes;
-        if (it > 0) {
-          if (!(ok = mbar_wait(p_full(0), (it - 1) & 1))) break;
-          if (!(ok = mbar_wait(v_full(ps), ((it - 1) / NS) & 1))) break;
+        const uint32_t vs = v_lo0 + ps * (kVTileBytes >> 4);
+        if constexpr (kSplitP) {
+          // Per query tile: S_t of this key tile once the softmax has loaded
+          // the previous S_t, then the PV of the previous key tile once its
+          // P_t is written.
+          if (it > 0 && !(ok = mbar_wait_warp(s_free(0), (it - 1) & 1))) break;
           tc_fence_after();
-          issue_pv<D>(tO0, tS0, vs, it > 1);
-        }
-        issue_qk<D>(tS0, sQ0, ks);
-        umma_commit(s_full(0));
-        if (has1) {
+          issue_qk<D>(tS0, q_lo0, ks);
+          umma_commit_e(s_full(0));
           if (it > 0) {
-            if (!(ok = mbar_wait(p_full(1), (it - 1) & 1))) break;
+            if (!(ok = mbar_wait_warp(p_full(0), (it - 1) & 1))) break;
+            if (!(ok = mbar_wait_warp(v_full(ps), ((it - 1) / NS) & 1))) break;
             tc_fence_after();
-            issue_pv<D>(tO1, tS1, vs, it > 1);
+            issue_pv<D>(tO0, tP0, vs, it > 1);
+            umma_commit_e(o_upd(0));
           }
-          issue_qk<D>(tS1, sQ0 + kTileBytes, ks);
-          umma_commit(s_full(1));
+          if (has1) {
+            if (it > 0 && !(ok = mbar_wait_warp(s_free(1), (it - 1) & 1))) break;
+            tc_fence_after();
+            issue_qk<D>(tS1, q_lo0 + (kTileBytes >> 4), ks);
+            umma_commit_e(s_full(1));
+            if (it > 0) {
+              if (!(ok = mbar_wait_warp(p_full(1), (it - 1) & 1))) break;
+              tc_fence_after();
+              issue_pv<D>(tO1, tP1, vs, it > 1);
+              umma_commit_e(o_upd(1));
+            }
+          }
+          umma_commit_e(k_empty(s));
+          if (it > 0) umma_commit_e(v_empty(ps));
+        } else {
+          if (it > 0) {
+            if (!(ok = mbar_wait_warp(p_full(0), (it - 1) & 1))) break;
+            if (!(ok = mbar_wait_warp(v_full(ps), ((it - 1) / NS) & 1))) break;
+            tc_fence_after();
+            issue_pv<D>(tO0, tP0, vs, it > 1);
+          }
+          issue_qk<D>(tS0, q_lo0, ks);
+          umma_commit_e(s_full(0));
+          if (has1) {
+            if (it > 0) {
+              if (!(ok = mbar_wait_warp(p_full(1), (it - 1) & 1))) break;
+              tc_fence_after();
+              issue_pv<D>(tO1, tP1, vs, it > 1);
+            }
+            issue_qk<D>(tS1, q_lo0 + (kTileBytes >> 4), ks);
+            umma_commit_e(s_full(1));
+          }
+          if (it > 0) umma_commit_e(v_empty(ps));
+          umma_commit_e(k_empty(s));
         }
-        if (it > 0) umma_commit(v_empty(ps));
-        umma_commit(k_empty(s));
       }
       if (ok) {
         const int ls = (tiles - 1) % NS;
-        const uint32_t vs = sV0 + ls * kVTileBytes;
-        ok = mbar_wait(p_full(0), (tiles - 1) & 1) && mbar_wait(v_full(ls), ((tiles - 1) / NS) & 1);
+        const uint32_t vs = v_lo0 + ls * (kVTileBytes >> 4);
+        ok = mbar_wait_warp(p_full(0), (tiles - 1) & 1) && mbar_wait_warp(v_full(ls), ((tiles - 1) / NS) & 1);
         if (ok) {
           tc_fence_after();
-          issue_pv<D>(tO0, tS0, vs, tiles > 1);
-          umma_commit(o_full(0));
-          if (has1 && mbar_wait(p_full(1), (tiles - 1) & 1)) {
+          issue_pv<D>(tO0, tP0, vs, tiles > 1);
+          umma_commit_e(o_full(0));
+          if (has1 && mbar_wait_warp(p_full(1), (tiles - 1) & 1)) {
             tc_fence_after();
-            issue_pv<D>(tO1, tS1, vs, tiles > 1);
-            umma_commit(o_full(1));
+            issue_pv<D>(tO1, tP1, vs, tiles > 1);
+            umma_commit_e(o_full(1));
           }
         }
       }
-      umma_commit(mma_done);
-      mbar_wait(mma_done, 0);
+      umma_commit_e(mma_done);
+      mbar_wait_warp(mma_done, 0);
     }
     __syncwarp();
   } else {
@@ -433,7 +485,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (t == 0 || has1) {
       const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
       const uint32_t tS = tmem_base + t * 128 + lane_off;
-      const uint32_t tO = tmem_base + 256 + t * 128 + lane_off;
+      const uint32_t tO = tmem_base + 256 + t * kOStride + lane_off;
+      const uint32_t tP = kSplitP ? tmem_base + 384 + t * 64 + lane_off : tS;
       const float scale_log2 = p.scale_log2;
       float m = -INFINITY;     // reference max, base-2 scaled units
       float l = 0.0f;          // row sum of the current chunk
@@ -447,6 +500,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc_fence_after();
         uint32_t sr[128];
         tmem_ld128_wait(tS, sr);
+        if constexpr (kSplitP) {
+          // S_t is in registers: the next QK^T may overwrite it.
+          tc_fence_before();
+          mbar_arrive(s_free(t));
+        }
         const int valid = kv.valid();
         if (valid < kBlockN) {
 #pragma unroll
@@ -480,6 +538,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           m = tmax;
         }
         const float neg_m = -m;
+        if constexpr (kSplitP) {
+          // P_t and O_t are free once the previous key tile's PV has completed.
+          if (it > 0) {
+            if (!(ok = mbar_wait_warp(o_upd(t), (it - 1) & 1))) break;
+            tc_fence_after();
+          }
+        }
         // P = 2^(S * scale - m): the affine part on packed pairs, 2^x on the
         // MUFU, row sum in four packed accumulators, P packed to bf16 pairs.
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -496,7 +561,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             add2(acc[2 * (j & 3)], acc[2 * (j & 3) + 1], a, b);
             pr[j] = pack_bf16x2(a, b);
           }
-          tmem_st16(tS + qtr * 16, pr);
+          tmem_st16(tP + qtr * 16, pr);
         }
         add2(acc[0], acc[1], acc[2], acc[3]);
         add2(acc[4], acc[5], acc[6], acc[7]);
