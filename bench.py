@@ -421,38 +421,46 @@ def run_ours(args):
     return 0
 
 
-def cfg_hbm_sweep(peaks, dev, numel=1 << 26, reps=10):
+def cfg_hbm_sweep(peaks, dev, sizes=(1 << 24, 1 << 26, 1 << 28), reps=10):
     """The CFG combine and its rel-MAE-fused form on operands larger than L2
-    (2^26 fp32 elements each: 768 MB of algorithmic traffic per call), outside
-    the timed step: the bandwidth figure the workload latents (L2-resident)
-    cannot show."""
+    (2^24, 2^26 and 2^28 fp32 elements each: 0.2, 0.8 and 3.2 GB of
+    algorithmic traffic per call), outside the timed step: the bandwidth
+    figure the workload latents (L2-resident) cannot show.  The top-level
+    figures are those of 2^26 elements; "sweep" holds every size."""
     import torch
     from sequence_attention_attn_b300 import dit_attn
-    g = torch.Generator(device=dev).manual_seed(5)
-    c = torch.randn(numel, generator=g, device=dev)
-    u = torch.randn(numel, generator=g, device=dev)
-    o = torch.empty_like(c)
-    sums = torch.empty(2, dtype=torch.float64, device=dev)
     stream = torch.cuda.current_stream()
-    res = {"numel_per_operand": numel, "bytes_per_call": 12.0 * numel, "l2": "operands larger than L2; no flush"}
-    for name, fn in (("cfg_combine", lambda: dit_attn.cfg_combine(c, u, 4.5, o, stream.cuda_stream)),
-                     ("cfg_combine_relmae", lambda: dit_attn.cfg_combine_relmae(c, u, 4.5, o, sums,
-                                                                                stream.cuda_stream))):
-        for _ in range(3):
-            fn()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(reps):
-            fn()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / reps
-        gbs = 12.0 * numel / (ms / 1e3) / 1e9
-        res[name] = {"ms": ms, "gbs": gbs, "frac_of_measured_hbm": gbs / peaks["hbm_gbs"],
-                     "frac_of_nominal_8000": gbs / NOMINAL_HBM_GBS}
-    res["rel_mae"] = float(sums[0] / sums[1])
-    del c, u, o
-    return res
+    sweep = []
+    for numel in sizes:
+        g = torch.Generator(device=dev).manual_seed(5)
+        c = torch.randn(numel, generator=g, device=dev)
+        u = torch.randn(numel, generator=g, device=dev)
+        o = torch.empty_like(c)
+        sums = torch.empty(2, dtype=torch.float64, device=dev)
+        res = {"numel_per_operand": numel, "bytes_per_call": 12.0 * numel, "l2": "operands larger than L2; no flush"}
+        for name, fn in (("cfg_combine", lambda: dit_attn.cfg_combine(c, u, 4.5, o, stream.cuda_stream)),
+                         ("cfg_combine_relmae", lambda: dit_attn.cfg_combine_relmae(c, u, 4.5, o, sums,
+                                                                                    stream.cuda_stream))):
+            for _ in range(3):
+                fn()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / reps
+            gbs = 12.0 * numel / (ms / 1e3) / 1e9
+            res[name] = {"ms": ms, "gbs": gbs, "frac_of_measured_hbm": gbs / peaks["hbm_gbs"],
+                         "frac_of_nominal_8000": gbs / NOMINAL_HBM_GBS}
+        res["rel_mae"] = float(sums[0] / sums[1])
+        sweep.append(res)
+        del c, u, o
+    torch.cuda.empty_cache()
+    main = next(r for r in sweep if r["numel_per_operand"] == 1 << 26) if (1 << 26) in sizes else sweep[-1]
+    return {**main, "sweep": [{"numel_per_operand": r["numel_per_operand"],
+                               "cfg_combine_gbs": r["cfg_combine"]["gbs"],
+                               "cfg_combine_relmae_gbs": r["cfg_combine_relmae"]["gbs"]} for r in sweep]}
 
 
 def torus_overlap(q, k, v, cfg, dev, n, reps=5):
