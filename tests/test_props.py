@@ -4,7 +4,9 @@ fp64 oracle (hypothesis, derandomised so every run draws the same cases).
 Shapes: B*H in 1..4, S in 1..700 (single keys, ragged tails, chunks shorter
 than a 128-key tile, chunk boundaries off tile boundaries), D in {64, 72, 128},
 1 <= n_kv_chunks <= min(S, 16), inputs N(0, std^2) with std in {0.5, 1, 2}.
-Also random LSE merges of 1..16 partials with some empty (-inf) chunks."""
+Also random LSE merges of 1..16 partials with some empty (-inf) chunks, random
+key ranges [j0, j1) of the range entry point, and the Torus-style chunked path
+with K/V streamed from pinned host memory."""
 import numpy as np
 import pytest
 import torch
@@ -77,3 +79,45 @@ def test_merge_random(n, rows, D, empty, seed):
     assert (np.isneginf(f64(lse)) == ~fin).all()
     if fin.any():
         assert np.abs(f64(lse)[fin] - ref_l[fin]).max() <= 1e-5 * max(1.0, np.abs(ref_l[fin]).max())
+
+
+@st.composite
+def range_case(draw):
+    B = draw(st.integers(1, 2))
+    H = draw(st.integers(1, 2))
+    S = draw(st.one_of(st.integers(1, 140), st.integers(120, 700)))
+    D = draw(st.sampled_from([64, 72, 128]))
+    j0 = draw(st.integers(0, S - 1))
+    j1 = draw(st.integers(j0 + 1, S))
+    std = draw(st.sampled_from([0.5, 1.0, 2.0]))
+    seed = draw(st.integers(0, 2**31 - 1))
+    return B, H, S, D, j0, j1, std, seed
+
+
+@SETTINGS
+@given(range_case())
+def test_key_range_random(case):
+    B, H, S, D, j0, j1, std, seed = case
+    q, k, v = workloads.make_random_qkv(B, H, S, D, seed=seed, std=std)
+    o_ref, l_ref = oracle.attention(f64(q), f64(k), f64(v), j0, j1)
+    qd, kd, vd = (t.to(DEV) for t in (q, k, v))
+    out, lse = dit_attn.attention_range(qd, kd, vd, j0, j1)
+    torch.cuda.synchronize()
+    assert dit_attn.dit_last_device_status() == 0
+    check_attention(out, lse, o_ref.reshape(-1, D), l_ref.reshape(-1),
+                    f"B={B} H={H} S={S} D={D} [{j0},{j1}) std={std}", scaled=True)
+
+
+@settings(max_examples=15, deadline=None, derandomize=True, database=None,
+          suppress_health_check=[HealthCheck.too_slow, HealthCheck.data_too_large])
+@given(attn_case())
+def test_torus_random(case):
+    B, H, S, D, n, std, seed = case
+    q, k, v = workloads.make_random_qkv(B, H, S, D, seed=seed, std=std)
+    o_ref, l_ref = oracle.attention(f64(q), f64(k), f64(v))
+    out, lse = dit_attn.attention_torus(q.to(DEV), k.pin_memory(), v.pin_memory(), n,
+                                        copy_stream=torch.cuda.Stream())
+    torch.cuda.synchronize()
+    assert dit_attn.dit_last_device_status() == 0
+    check_attention(out, lse, o_ref.reshape(-1, D), l_ref.reshape(-1),
+                    f"torus B={B} H={H} S={S} D={D} n={n} std={std}", scaled=True)
