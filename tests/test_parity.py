@@ -179,6 +179,27 @@ def test_attention_full_size_sampled(name, n):
                     lse.reshape(-1)[torch.as_tensor(rows, device=DEV)], o_ref, l_ref, f"{name} n={n}")
 
 
+def test_attention_offsets_past_32_bits_sampled():
+    # B*H*S*D = 2.18e9 elements (4.4 GB per tensor): element offsets of the
+    # last heads pass 2^31 and byte offsets pass 2^32.
+    B, H, S, D = 1, 520, 65536, 64
+    q, k, v = workloads.make_random_qkv(B, H, S, D, seed=77, device=DEV)
+    out, lse = dit_attn.attention(q, k, v, n_kv_chunks=4)
+    torch.cuda.synchronize()
+    assert_no_device_error()
+    rng = np.random.default_rng(3)
+    rows = []
+    for bh in (0, 260, H - 2, H - 1):
+        rows += [bh * S + r for r in (0, 1, 127, 128, S // 4, S // 4 + 1, S - 129, S - 1)]
+        rows += [bh * S + int(r) for r in rng.integers(0, S, 4)]
+    rows = np.array(sorted(set(rows)), dtype=np.int64)
+    o_ref, l_ref = oracle_rows(q, k, v, rows)
+    idx = torch.as_tensor(rows, device=DEV)
+    check_attention(out.reshape(-1, D)[idx], lse.reshape(-1)[idx], o_ref, l_ref, "offsets past 32 bits")
+    del q, k, v, out, lse
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("S", [1, 2, 100, 127, 128, 129, 255, 257, 383, 640])
 @pytest.mark.parametrize("D", [64, 72, 128])
 def test_attention_edge_lengths(S, D):
