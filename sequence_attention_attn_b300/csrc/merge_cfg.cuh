@@ -59,16 +59,20 @@ __global__ void __launch_bounds__(kStreamThreads)
     if (lse != -INFINITY) {
       const float4 *src = reinterpret_cast<const float4 *>(partials) + r * d4 + c4;
       const long long cstride = rows * d4;
-#pragma unroll 4
+      // Loads issued for every chunk (the buffer is in bounds for all of
+      // them) so that eight are in flight at once; an empty chunk's partial
+      // is loaded but never used.
+#pragma unroll 8
       for (int c = 0; c < n; ++c) {
         const float l = __ldg(lses + c * rows + r);
-        if (l == -INFINITY) continue;
-        const float w = __expf(l - lse);
         const float4 v = ld_stream(src + c * cstride);
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
+        if (l != -INFINITY) {
+          const float w = __expf(l - lse);
+          acc.x = fmaf(w, v.x, acc.x);
+          acc.y = fmaf(w, v.y, acc.y);
+          acc.z = fmaf(w, v.z, acc.z);
+          acc.w = fmaf(w, v.w, acc.w);
+        }
       }
     }
     st_stream(reinterpret_cast<float4 *>(out) + idx, acc);
