@@ -93,10 +93,11 @@ __global__ void __launch_bounds__(kStreamThreads)
     const float lse = merged_lse(lses, n, rows, r);
     float acc = 0.0f;
     if (lse != -INFINITY) {
+#pragma unroll 8
       for (int c = 0; c < n; ++c) {
         const float l = __ldg(lses + c * rows + r);
-        if (l == -INFINITY) continue;
-        acc = fmaf(__expf(l - lse), __ldg(partials + (c * rows + r) * D + d), acc);
+        const float v = __ldg(partials + (c * rows + r) * D + d);  // in bounds; unused if the chunk is empty
+        if (l != -INFINITY) acc = fmaf(__expf(l - lse), v, acc);
       }
     }
     out[idx] = acc;
