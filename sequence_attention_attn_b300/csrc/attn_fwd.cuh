@@ -19,8 +19,9 @@
 //               from a single lane inside a divergent branch cost about twice
 //               as many cycles per MMA.
 //   warps 2-5   softmax for query tile 0, warps 6-9 for query tile 1.  Each
-//               thread owns one query row (one TMEM lane): it loads its S row,
-//               takes the row max, rescales its O row in TMEM when the
+//               thread owns one query row (one TMEM lane): it loads its S row
+//               with the reducing TMEM load that also returns the row max
+//               (sm_103a), rescales its O row in TMEM when the
 //               reference max has to move, writes P = 2^(S*scale - m) as bf16
 //               and keeps the row sum.
 // TMEM columns: S_t at 128 t.  D = 64: O_t at 256 + 64 t and P_t at
@@ -499,30 +500,34 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (!(ok = mbar_wait_warp(s_full(t), it & 1))) break;
         tc_fence_after();
         uint32_t sr[128];
-        tmem_ld128_wait(tS, sr);
+        float hw_max;  // max of the 128 loaded columns, from the reducing load
+        tmem_ld128_max_wait(tS, sr, hw_max);
         if constexpr (kSplitP) {
           // S_t is in registers: the next QK^T may overwrite it.
           tc_fence_before();
           mbar_arrive(s_free(t));
         }
         const int valid = kv.valid();
+        float row_max = hw_max;
         if (valid < kBlockN) {
+          // A tile cut at a chunk end or at S: the columns past `valid` are
+          // masked to -inf and the max is taken again over the rest (eight
+          // independent chains of 3-input max).
 #pragma unroll
           for (int j = 0; j < kBlockN; ++j)
             if (j >= valid) sr[j] = __float_as_uint(-INFINITY);
+          float mx[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(sr[i]);
+#pragma unroll
+          for (int j = 8; j < kBlockN; j += 16) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              mx[i] = max3(mx[i], __uint_as_float(sr[j + i]), __uint_as_float(sr[j + 8 + i]));
+          }
+          row_max = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
         }
-        // Row max: eight independent chains of 3-input max.
-        float mx[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(sr[i]);
-#pragma unroll
-        for (int j = 8; j < kBlockN; j += 16) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            mx[i] = max3(mx[i], __uint_as_float(sr[j + i]), __uint_as_float(sr[j + 8 + i]));
-        }
-        const float tmax =
-            max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * scale_log2;
+        const float tmax = row_max * scale_log2;
         float o_scale = 1.0f;
         if (kv.chunk_start() && it > 0) {
           // The previous chunk is complete: fold its LSE into the running one.

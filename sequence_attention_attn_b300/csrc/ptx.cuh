@@ -197,6 +197,33 @@ __device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]
       : "memory");
 }
 
+// 128 columns in four x32 reducing loads (tcgen05.ld.red, sm_103a), one wait:
+// besides the values, each load returns the max of its 32 columns in this
+// thread's lane; mx is the max of the four.
+__device__ __forceinline__ void tmem_ld128_max_wait(uint32_t taddr, uint32_t (&r)[128], float &mx) {
+  float m0, m1, m2, m3;
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %128, [%132];\n\t"
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+      "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, %129, [%133];\n\t"
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+      "{%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
+      "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, %130, [%134];\n\t"
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+      "{%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,"
+      "%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, %131, [%135];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : DITK_R8(0), DITK_R8(8), DITK_R8(16), DITK_R8(24), DITK_R8(32), DITK_R8(40), DITK_R8(48), DITK_R8(56),
+        DITK_R8(64), DITK_R8(72), DITK_R8(80), DITK_R8(88), DITK_R8(96), DITK_R8(104), DITK_R8(112), DITK_R8(120),
+        "=f"(m0), "=f"(m1), "=f"(m2), "=f"(m3)
+      : "r"(taddr), "r"(taddr + 32), "r"(taddr + 64), "r"(taddr + 96)
+      : "memory");
+  mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+}
+
 // 128 columns in four x32 loads, one wait.
 __device__ __forceinline__ void tmem_ld128_wait(uint32_t taddr, uint32_t (&r)[128]) {
   asm volatile(
