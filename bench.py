@@ -554,13 +554,27 @@ def run_e2e(args, q, k, v, parts, part_lse, eps_c, eps_u, out, lse, m_out, m_lse
     h2d = sum(t.numel() * t.element_size() for t in ins)
     d2h = sum(t.numel() * t.element_size() for t in outs)
 
+    side = torch.cuda.Stream(device=dev)
+    landed = torch.cuda.Event()
+
     def one():
-        for d, h in zip(ins, h_in):
+        # q, k, v on the compute stream; the merge and CFG inputs on a side
+        # stream, so that their copy overlaps the attention, and the attention
+        # output is read back while they are still coming in.
+        side.wait_stream(stream)
+        for d, h in zip(ins[:3], h_in[:3]):
             d.copy_(h, non_blocking=True)
+        with torch.cuda.stream(side):
+            for d, h in zip(ins[3:], h_in[3:]):
+                d.copy_(h, non_blocking=True)
+            landed.record(side)
         dit_attn.dit_attn_fwd(q, k, v, out, lse, n, sptr)
+        for h, d in zip(h_out[:2], outs[:2]):
+            h.copy_(d, non_blocking=True)
+        stream.wait_event(landed)
         dit_attn.dit_attn_merge(parts, part_lse, m_out, m_lse, sptr)
         dit_attn.cfg_combine(eps_c, eps_u, cfg.cfg_w, c_out, sptr)
-        for h, d in zip(h_out, outs):
+        for h, d in zip(h_out[2:], outs[2:]):
             h.copy_(d, non_blocking=True)
 
     one()
