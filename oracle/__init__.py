@@ -169,14 +169,25 @@ class OracleLib:
 
     def cfg_relmae(self, eps_c, eps_u, w: float):
         """CFG combine plus the rel-MAE sums.  Returns (out, (sum |eps_c - eps_u|,
-        sum |eps_u|)); the rel-MAE is their ratio."""
+        sum |eps_u|)); the rel-MAE is their ratio (``cfg_relmae_ratio``)."""
         eps_c, eps_u = _as_f64(eps_c), _as_f64(eps_u)
         if eps_c.shape != eps_u.shape:
             raise ValueError("eps_c and eps_u must share one shape")
         out = np.empty_like(eps_c)
-        sums = np.zeros(2, dtype=np.float64)
+        sums = np.zeros(3, dtype=np.float64)
         self._lib.oracle_cfg_relmae(_p(eps_c), _p(eps_u), float(w), _p(out), eps_c.size, _p(sums))
         return out, (float(sums[0]), float(sums[1]))
+
+    def cfg_relmae_ratio(self, eps_c, eps_u):
+        """The rel-MAE sum |eps_c - eps_u| / sum |eps_u| as the oracle computes it
+        (0 when both sums are 0, +inf when only the base sum is)."""
+        eps_c, eps_u = _as_f64(eps_c), _as_f64(eps_u)
+        if eps_c.shape != eps_u.shape:
+            raise ValueError("eps_c and eps_u must share one shape")
+        out = np.empty_like(eps_c)
+        sums = np.zeros(3, dtype=np.float64)
+        self._lib.oracle_cfg_relmae(_p(eps_c), _p(eps_u), 0.0, _p(out), eps_c.size, _p(sums))
+        return float(sums[2])
 
     def attention_chunked(self, q, k, v, bounds):
         """Chunked attention: (O_c, LSE_c) per key range in ``bounds``, then the
@@ -238,6 +249,10 @@ def cfg_combine(eps_c, eps_u, w: float):
 
 def cfg_relmae(eps_c, eps_u, w: float):
     return default().cfg_relmae(eps_c, eps_u, w)
+
+
+def cfg_relmae_ratio(eps_c, eps_u):
+    return default().cfg_relmae_ratio(eps_c, eps_u)
 
 
 def attention_chunked(q, k, v, bounds):

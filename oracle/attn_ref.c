@@ -37,8 +37,10 @@
  *    named rel-MAE there without a formula.  Plainest reading: the mean
  *    absolute difference relative to the mean absolute unconditional noise,
  *        rel-MAE = sum_i |eps_c[i] - eps_u[i]| / sum_i |eps_u[i]|,
- *    computed in the same pass as the combine; the two sums are returned and
- *    their ratio is the rel-MAE.
+ *    computed in the same pass as the combine.  The two sums and their ratio
+ *    are returned.  The page does not say what happens when the unconditional
+ *    noise is all zero; the reading taken is the limit of identical paths:
+ *    0 when the difference sum is 0 too, +inf otherwise.
  *
  * Layouts: q, k, v, out are [BH][S][D] row-major doubles; lse is [BH][S].
  * Every loop is the definition written out, with no blocking or reordering.
@@ -165,8 +167,9 @@ int oracle_cfg_combine(const double *eps_c, const double *eps_u, double w,
   return 0;
 }
 
-/* Classifier-free guidance combine plus the two sums of the rel-MAE
- * discrepancy: sums[0] = sum |eps_c - eps_u|, sums[1] = sum |eps_u|. */
+/* Classifier-free guidance combine plus the rel-MAE discrepancy:
+ * sums[0] = sum |eps_c - eps_u|, sums[1] = sum |eps_u|,
+ * sums[2] = sums[0] / sums[1] (0 if both are 0, +inf if only sums[1] is). */
 int oracle_cfg_relmae(const double *eps_c, const double *eps_u, double w,
                       double *out, long long numel, double *sums) {
   if (numel < 0) return -1;
@@ -179,6 +182,10 @@ int oracle_cfg_relmae(const double *eps_c, const double *eps_u, double w,
   }
   sums[0] = diff;
   sums[1] = base;
+  if (base > 0.0)
+    sums[2] = diff / base;
+  else
+    sums[2] = diff == 0.0 ? 0.0 : INFINITY;
   return 0;
 }
 

@@ -219,11 +219,16 @@ def pin_cfg_relmae(impl):
     exact integer in fp64); eps_c = eps_u gives 0, eps_c = 2 eps_u gives a
     ratio of exactly 1, eps_c = -eps_u exactly 2; the ratio is scale
     invariant; the fused combine equals the plain one; the sums match the
-    NumPy twin."""
+    NumPy twin.  The ratio: 8 / 10 on the integer case; 0 / 0 gives 0 and
+    x / 0 gives +inf (all-zero unconditional noise)."""
     u = np.array([1.0, -2.0, 3.0, -4.0])
     c = np.array([2.0, 0.0, 3.0, 1.0])          # |c - u| = 1, 2, 0, 5
     _, (d, b) = impl.cfg_relmae(c, u, 4.5)
     assert (d, b) == (8.0, 10.0), (d, b)
+    assert impl.cfg_relmae_ratio(c, u) == 0.8
+    z = np.zeros(5)
+    assert impl.cfg_relmae_ratio(z, z) == 0.0
+    assert impl.cfg_relmae_ratio(np.array([0.0, 0.0, -0.5, 0.0, 0.0]), z) == math.inf
     rng = np.random.default_rng(24)
     u = _rand(rng, 3, 16, 16)
     _, (d, b) = impl.cfg_relmae(u, u, 2.0)
@@ -232,6 +237,9 @@ def pin_cfg_relmae(impl):
     assert d == b, (d, b)
     _, (d, b) = impl.cfg_relmae(-u, u, 2.0)
     assert d == 2.0 * b, (d, b)
+    assert impl.cfg_relmae_ratio(u, u) == 0.0
+    assert impl.cfg_relmae_ratio(2.0 * u, u) == 1.0
+    assert impl.cfg_relmae_ratio(-u, u) == 2.0
     c = _rand(rng, 3, 16, 16)
     out, (d, b) = impl.cfg_relmae(c, u, 4.5)
     _, (d3, b3) = impl.cfg_relmae(3.0 * c, 3.0 * u, 4.5)

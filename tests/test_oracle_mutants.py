@@ -40,6 +40,8 @@ MUTANTS = [
     ("relmae_signed_difference", "diff += fabs(d);", "diff += d;"),
     ("relmae_difference_of_base", "diff += fabs(d);", "diff += fabs(eps_u[i]);"),
     ("relmae_combine_sign", "out[i] = eps_u[i] + w * d;", "out[i] = eps_u[i] - w * d;"),
+    ("relmae_ratio_inverted", "sums[2] = diff / base;", "sums[2] = base / diff;"),
+    ("relmae_zero_base_finite", "diff == 0.0 ? 0.0 : INFINITY;", "0.0;"),
 ]
 
 
