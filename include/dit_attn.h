@@ -102,10 +102,9 @@ dit_status dit_attn_fwd_partials(const void *q, const void *k, const void *v,
  *     LSE_i = ln sum_{j0 <= j < j1} exp(s_ij),
  *     out_i = sum_{j0 <= j < j1} exp(s_ij - LSE_i) v_j.
  *
- *   q, k, v      bf16 [B, H, S, D] as for dit_attn_fwd (only key rows
- *                [j0, j1) of k and v are read, plus the rest of the last
- *                128-key tile, whose weights are masked to 0 but which must
- *                hold finite values).
+ *   q, k, v      bf16 [B, H, S, D] as for dit_attn_fwd.  Only key rows
+ *                [j0, j1) of k and v are read; the other rows may hold
+ *                anything (NaN included) or still be in flight.
  *   out          fp32 [B * H * S, D], 16-byte aligned.
  *   lse          fp32 [B * H * S], 16-byte aligned.
  *   j0, j1       0 <= j0 < j1 <= S (else DIT_ERR_INVALID_ARG).
@@ -119,8 +118,8 @@ dit_status dit_attn_fwd_range(const void *q, const void *k, const void *v,
  * rows of chunk c (the balanced partition of dit_attn_fwd) are copied from
  * k_src / v_src into k / v on copy_stream, one event per chunk, and chunk c
  * is computed on stream (dit_attn_fwd_range into partials[c], lses[c]) as
- * soon as its rows -- and those of any later chunk its last tile reaches --
- * have arrived, while later chunks are still being copied; then
+ * soon as its own rows have arrived, while later chunks are still being
+ * copied; then
  * dit_attn_merge combines the partials into out / lse_out.  Source:
  * "SwiftFusion ..." (idea 2: Torus attention splits a received block into
  * pieces and computes piece i while piece i + 1 arrives); on one GPU the
@@ -189,21 +188,27 @@ dit_status cfg_combine(const float *eps_c, const float *eps_u, float w,
  * sum |eps_c - eps_u| / sum |eps_u|).
  *
  *   eps_c, eps_u, out, numel, w   as for cfg_combine (out may alias an input).
- *   sums   fp64 [2] device, 8-byte aligned, not overlapping the other buffers:
- *          set to {sum |eps_c - eps_u|, sum |eps_u|} (zeroed by this call
- *          before the kernel runs); the rel-MAE is sums[0] / sums[1].  The
- *          sums are accumulated in fp32 per thread and fp64 beyond, in an order
- *          that may vary between calls in the last bits.
+ *   sums   fp64 [3] device, 8-byte aligned, not overlapping the other buffers:
+ *          set to {sum |eps_c - eps_u|, sum |eps_u|, rel-MAE} with
+ *          rel-MAE = sums[0] / sums[1], computed on the device; an all-zero
+ *          eps_u gives 0 when eps_c == eps_u everywhere and +inf otherwise.
+ *          This call zeroes the three values before its kernel runs; while
+ *          the kernel runs, sums[2] holds its count of finished blocks.  The
+ *          sums are accumulated in fp32 per thread and fp64 beyond, in an
+ *          order that may vary between calls in the last bits.
  */
 dit_status cfg_combine_relmae(const float *eps_c, const float *eps_u, float w,
                               float *out, long long numel, double *sums,
                               dit_stream_t stream);
 
 /*
- * dit_last_device_status -- synchronises `stream`, then reads and clears this
- * device's status word.  Returns DIT_ERR_DEVICE_TIMEOUT if a kernel gave up on
- * a bounded wait since the last call, DIT_ERR_CUDA if the synchronisation
- * itself failed, else DIT_OK.
+ * dit_last_device_status -- after the work queued on `stream`, reads and
+ * clears this device's status word in one atomic exchange (a one-thread
+ * kernel on `stream`), then synchronises `stream`.  Returns
+ * DIT_ERR_DEVICE_TIMEOUT if a kernel gave up on a bounded wait since the last
+ * call, DIT_ERR_CUDA if the copy or the synchronisation failed, else DIT_OK.
+ * A timeout recorded by a kernel on another stream after the exchange stays
+ * in the word for the next call.
  */
 dit_status dit_last_device_status(dit_stream_t stream);
 

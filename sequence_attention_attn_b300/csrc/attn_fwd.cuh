@@ -382,13 +382,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       // Drain: every load issued must land before the CTA may exit.  Waiting on
       // the parity of a stage's last use returns at once if it already landed.
+      // These waits ignore the device status word (see ptx.cuh).
 #pragma unroll
       for (int s = 0; s < NS; ++s) {
-        if (k_last[s] >= 0) mbar_wait(k_full(s), k_last[s] & 1);
-        if (v_last[s] >= 0) mbar_wait(v_full(s), v_last[s] & 1);
+        if (k_last[s] >= 0) mbar_wait_drain(k_full(s), k_last[s] & 1);
+        if (v_last[s] >= 0) mbar_wait_drain(v_full(s), v_last[s] & 1);
       }
-      if (has1) mbar_wait(q_full(1), 0);
-      mbar_wait(q_full(0), 0);
+      if (has1) mbar_wait_drain(q_full(1), 0);
+      mbar_wait_drain(q_full(0), 0);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -474,8 +475,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
         }
       }
+      // Every MMA this warp issued completes before TMEM is freed.
       umma_commit_e(mma_done);
-      mbar_wait_warp(mma_done, 0);
+      mbar_wait_drain_warp(mma_done, 0);
     }
     __syncwarp();
   } else {

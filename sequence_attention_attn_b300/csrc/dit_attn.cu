@@ -22,7 +22,7 @@
 
 namespace {
 
-constexpr int kAbiVersion = 1;
+constexpr int kAbiVersion = 2;
 constexpr int kMaxDevices = 64;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -47,6 +47,8 @@ struct DeviceState {
 std::mutex g_mu;
 // Serialises dit_attn_fwd_torus calls: they share one event pool per device.
 std::mutex g_torus_mu;
+// Serialises status reads: they share the device word the exchange writes to.
+std::mutex g_status_mu;
 DeviceState g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -96,10 +98,12 @@ dit_status get_encoder() {
   return DIT_OK;
 }
 
-// 3-D bf16 view [BH][S][D] of one of q, k, v; a box of `box_cols` x 128 rows.
-dit_status encode_qkv_map(CUtensorMap *map, const void *ptr, long long BH, int S, int D, int box_cols,
+// 3-D bf16 view [BH][rows][D] of one of q, k, v (head stride S rows); a box
+// of `box_cols` x 128 rows.  Rows >= `rows` of a head are never read: TMA
+// fills them with zeros.
+dit_status encode_qkv_map(CUtensorMap *map, const void *ptr, long long BH, int S, int rows, int D, int box_cols,
                           CUtensorMapSwizzle swz) {
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S),
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows),
                         static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(S) * D * 2};
   cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(ditk::kBlockM), 1};
@@ -137,16 +141,19 @@ dit_status launch_attn(DeviceState &st, int didx, const void *q, const void *k, 
   }
   CUtensorMap mq, mq_t, mk, mk_t, mv, mv_t;
   dit_status s;
-  if ((s = encode_qkv_map(&mq, q, BH, S, D, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != DIT_OK) return s;
-  if ((s = encode_qkv_map(&mk, k, BH, S, D, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != DIT_OK) return s;
-  if ((s = encode_qkv_map(&mv, v, BH, S, D, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != DIT_OK) return s;
+  // A key range [j0, j1) maps only the key rows below j1, so the masked tail
+  // of its last tile is zero-filled by TMA instead of read.
+  const int kv_rows = prm.key_j1 > 0 ? prm.key_j1 : S;
+  if ((s = encode_qkv_map(&mq, q, BH, S, S, D, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != DIT_OK) return s;
+  if ((s = encode_qkv_map(&mk, k, BH, S, kv_rows, D, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != DIT_OK) return s;
+  if ((s = encode_qkv_map(&mv, v, BH, S, kv_rows, D, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != DIT_OK) return s;
   // Columns 64.. of Q and K: a 16-column 32-byte-swizzled box for D = 72 (the
   // last K step of QK^T), the main map's 64-column box otherwise.  V always
   // takes the main map's box at column 64 (D = 72: columns 72..127 of that box
   // are zero-filled, and PV runs with N = 80).
   if (D == 72) {
-    if ((s = encode_qkv_map(&mq_t, q, BH, S, D, 16, CU_TENSOR_MAP_SWIZZLE_32B)) != DIT_OK) return s;
-    if ((s = encode_qkv_map(&mk_t, k, BH, S, D, 16, CU_TENSOR_MAP_SWIZZLE_32B)) != DIT_OK) return s;
+    if ((s = encode_qkv_map(&mq_t, q, BH, S, S, D, 16, CU_TENSOR_MAP_SWIZZLE_32B)) != DIT_OK) return s;
+    if ((s = encode_qkv_map(&mk_t, k, BH, S, kv_rows, D, 16, CU_TENSOR_MAP_SWIZZLE_32B)) != DIT_OK) return s;
   } else {
     mq_t = mq;
     mk_t = mk;
@@ -319,7 +326,8 @@ dit_status dit_attn_fwd_torus(const void *q, const void *k_src, const void *v_sr
   }
   if (ranges_overlap(k, kv_bytes, v, kv_bytes) || ranges_overlap(k, kv_bytes, q, kv_bytes) ||
       ranges_overlap(v, kv_bytes, q, kv_bytes) || ranges_overlap(k_src, kv_bytes, k, kv_bytes) ||
-      ranges_overlap(v_src, kv_bytes, v, kv_bytes) || ranges_overlap(lses, l_bytes, partials, p_bytes))
+      ranges_overlap(v_src, kv_bytes, v, kv_bytes) || ranges_overlap(k_src, kv_bytes, v, kv_bytes) ||
+      ranges_overlap(v_src, kv_bytes, k, kv_bytes) || ranges_overlap(lses, l_bytes, partials, p_bytes))
     return DIT_ERR_INVALID_ARG;
   int dev = 0;
   DeviceState *st = nullptr;
@@ -355,20 +363,12 @@ dit_status dit_attn_fwd_torus(const void *q, const void *k_src, const void *v_sr
       return DIT_ERR_CUDA;
     if (cudaEventRecord(ev[c], xs) != cudaSuccess) return DIT_ERR_CUDA;
   }
-  // Chunk c is computed once its rows have arrived.  Its last 128-key tile
-  // also reads (and masks) rows past the chunk end, which must hold finished
-  // data (a masked weight of 0 times an unfinished NaN is NaN), so the wait
-  // covers every chunk that tile reaches.
-  const long long tile = ditk::kBlockN;
-  int waited = -1;
+  // Chunk c is computed as soon as its own rows have arrived: the key-range
+  // kernel reads no row at or past the chunk end (TMA zero-fills the tail of
+  // its last tile), so later chunks may still be in flight.
   for (int c = 0; c < n; ++c) {
     const long long j0 = bound(c), j1 = bound(c + 1);
-    const long long reach = std::min<long long>(S, j0 + (j1 - j0 + tile - 1) / tile * tile) - 1;
-    int last = c;
-    while (last + 1 < n && bound(last + 1) <= reach) ++last;
-    for (int w = waited + 1; w <= last; ++w)
-      if (cudaStreamWaitEvent(cs, ev[w], 0) != cudaSuccess) return DIT_ERR_CUDA;
-    waited = std::max(waited, last);
+    if (cudaStreamWaitEvent(cs, ev[c], 0) != cudaSuccess) return DIT_ERR_CUDA;
     s = attn_dispatch<true>(q, k, v, nullptr, nullptr, partials + static_cast<size_t>(c) * rows * D,
                             lses + static_cast<size_t>(c) * rows, B, H, S, D, 1, stream, static_cast<int>(j0),
                             static_cast<int>(j1));
@@ -448,15 +448,15 @@ dit_status cfg_combine_relmae(const float *eps_c, const float *eps_u, float w, f
   // out may be exactly eps_c or eps_u; any other overlap is an error.
   const size_t bytes = static_cast<size_t>(numel) * 4;
   if ((out != eps_c && ranges_overlap(out, bytes, eps_c, bytes)) ||
-      (out != eps_u && ranges_overlap(out, bytes, eps_u, bytes)) || ranges_overlap(sums, 16, eps_c, bytes) ||
-      ranges_overlap(sums, 16, eps_u, bytes) || ranges_overlap(sums, 16, out, bytes))
+      (out != eps_u && ranges_overlap(out, bytes, eps_u, bytes)) || ranges_overlap(sums, 24, eps_c, bytes) ||
+      ranges_overlap(sums, 24, eps_u, bytes) || ranges_overlap(sums, 24, out, bytes))
     return DIT_ERR_INVALID_ARG;
   int dev = 0;
   DeviceState *st = nullptr;
   dit_status s = select_device(stream, &dev, &st);
   if (s != DIT_OK) return s;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(sums, 0, 2 * sizeof(double), cs) != cudaSuccess) return DIT_ERR_CUDA;
+  if (cudaMemsetAsync(sums, 0, 3 * sizeof(double), cs) != cudaSuccess) return DIT_ERR_CUDA;
   const long long n4 = numel / 4;
   const int grid = stream_grid(*st, n4 > 0 ? n4 : 1);
   ditk::cfg_combine_relmae_kernel<<<grid, ditk::kStreamThreads, 0, cs>>>(eps_c, eps_u, w, out, numel, sums);
@@ -477,15 +477,18 @@ dit_status dit_last_device_status(dit_stream_t stream) {
   DeviceState *st = nullptr;
   dit_status s = select_device(stream, &dev, &st);
   if (s != DIT_OK) return s;
-  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return DIT_ERR_CUDA;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lock(g_status_mu);
+  // After the work queued on the stream: take the word (read and clear in one
+  // atomic exchange on the device), then copy what was taken back.
+  ditk::status_take_kernel<<<1, 1, 0, cs>>>();
+  if (cudaGetLastError() != cudaSuccess) return DIT_ERR_LAUNCH;
   unsigned int word = 0;
-  if (cudaMemcpyFromSymbol(&word, ditk::g_status, sizeof(word)) != cudaSuccess) return DIT_ERR_CUDA;
-  if (word != 0u) {
-    const unsigned int zero = 0u;
-    if (cudaMemcpyToSymbol(ditk::g_status, &zero, sizeof(zero)) != cudaSuccess) return DIT_ERR_CUDA;
-    return DIT_ERR_DEVICE_TIMEOUT;
-  }
-  return DIT_OK;
+  if (cudaMemcpyFromSymbolAsync(&word, ditk::g_status_taken, sizeof(word), 0, cudaMemcpyDeviceToHost, cs) !=
+      cudaSuccess)
+    return DIT_ERR_CUDA;
+  if (cudaStreamSynchronize(cs) != cudaSuccess) return DIT_ERR_CUDA;
+  return word != 0u ? DIT_ERR_DEVICE_TIMEOUT : DIT_OK;
 }
 
 }  // extern "C"

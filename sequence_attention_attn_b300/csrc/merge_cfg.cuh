@@ -10,9 +10,9 @@
 //   and unconditional paths of classifier-free guidance ("Accelerating
 //   Diffusion via Hybrid Data-Pipeline Parallelism Based on Conditional
 //   Guidance Scheduling", Technische Zusammenfassung 2A).
-// cfg_combine_relmae: the same combine plus, in the same pass, the two sums
-//   of the rel-MAE discrepancy between the paths that the same page (2B)
-//   switches its parallelism phases on: sum |eps_c - eps_u| and sum |eps_u|.
+// cfg_combine_relmae: the same combine plus, in the same pass, the rel-MAE
+//   discrepancy between the paths that the same page (2B) switches its
+//   parallelism phases on: sum |eps_c - eps_u|, sum |eps_u| and their ratio.
 //
 // Both are pure streams: each output element is written once and each input
 // element read once, 16 bytes per thread access, consecutive threads on
@@ -122,7 +122,15 @@ __global__ void __launch_bounds__(kStreamThreads)
   }
 }
 
+// rel-MAE = diff / base; an all-zero base gives 0 when diff is 0 too (the
+// paths are identical) and +inf otherwise.  NaN inputs stay NaN.
+__device__ __forceinline__ double relmae_ratio(double diff, double base) {
+  return (base == 0.0 && diff == 0.0) ? 0.0 : diff / base;
+}
+
 // Sums of a (diff, base) pair over the block, added to sums[0..1] in fp64.
+// sums[2] (zero on entry) counts the finished blocks while the grid runs; the
+// last block to finish overwrites it with the ratio of the two totals.
 __device__ __forceinline__ void block_add_sums(double diff, double base, double *sums) {
   __shared__ double red[2][kStreamThreads / 32];
 #pragma unroll
@@ -144,12 +152,20 @@ __device__ __forceinline__ void block_add_sums(double diff, double base, double 
     }
     atomicAdd(sums, d);
     atomicAdd(sums + 1, b);
+    __threadfence();
+    unsigned long long *done = reinterpret_cast<unsigned long long *>(sums + 2);
+    if (atomicAdd(done, 1ull) == gridDim.x - 1) {
+      // Every other block's sums were added before its count.
+      __threadfence();
+      const double total_d = atomicAdd(sums, 0.0), total_b = atomicAdd(sums + 1, 0.0);
+      sums[2] = relmae_ratio(total_d, total_b);
+    }
   }
 }
 
 // One thread per float4 (grid-stride), the numel % 4 tail by the first
 // threads; per-thread sums in fp32 (one accumulator per lane of the float4),
-// fp64 from the warp level on.  sums must be zero on entry.  out may alias
+// fp64 from the warp level on.  sums[0..2] must be zero on entry.  out may alias
 // eps_c or eps_u (each element is read and then written by the same thread).
 __global__ void __launch_bounds__(kStreamThreads)
     cfg_combine_relmae_kernel(const float *eps_c, const float *eps_u, float w, float *out, long long numel,

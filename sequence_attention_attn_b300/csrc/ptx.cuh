@@ -5,7 +5,11 @@
 // Every wait on an mbarrier is bounded: after ~1 s of device time it records a
 // code in the device status word and returns false, so that a logic error
 // ends the kernel with an error status instead of hanging the GPU.  Once the
-// status word is non-zero every later slow-path wait gives up immediately.
+// status word is non-zero every later main-loop wait gives up soon after.
+// Drain waits -- the ones a CTA makes before it frees TMEM or exits, on its
+// own TMA loads and MMAs in flight -- ignore the status word and honour only
+// their own time limit: those operations complete by themselves, and a CTA
+// must not release memory they still write.
 #pragma once
 #include <cstdint>
 #include <cuda.h>
@@ -14,6 +18,8 @@ namespace ditk {
 
 // Device status word (one per device; read and cleared by the host).
 __device__ unsigned int g_status;
+// The value the last status read took out of g_status (see status_take_kernel).
+__device__ unsigned int g_status_taken;
 
 constexpr unsigned int kStatusTimeout = 1u;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
@@ -60,14 +66,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits until the phase with the given parity has completed.  Returns false
-// (and sets the status word) if that takes longer than kWaitLimitNs or if
-// another wait anywhere on the device has already given up.
+// (and sets the status word) if that takes longer than kWaitLimitNs.  With
+// kHonourStatus it also returns false once another wait anywhere on the
+// device has given up (main-loop waits); without it only its own time limit
+// ends it (drain waits).
+template <bool kHonourStatus>
 __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     for (int i = 0; i < 256; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (*reinterpret_cast<volatile unsigned int *>(&g_status) != 0u) return false;
+    if (kHonourStatus && *reinterpret_cast<volatile unsigned int *>(&g_status) != 0u) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       atomicOr(&g_status, kStatusTimeout);
       return false;
@@ -77,12 +86,22 @@ __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity) {
 
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity);
+  return mbar_wait_slow<true>(bar, parity);
+}
+
+// A wait on the CTA's own asynchronous work before it exits or frees TMEM.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow<false>(bar, parity);
 }
 
 // Warp-uniform wait: every lane polls, and the warp proceeds only if all did.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity) {
   const bool ok = mbar_wait(bar, parity);
+  return __all_sync(0xffffffffu, ok);
+}
+__device__ __forceinline__ bool mbar_wait_drain_warp(uint32_t bar, uint32_t parity) {
+  const bool ok = mbar_wait_drain(bar, parity);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -95,6 +114,11 @@ __global__ void selftest_wait_kernel() {
   fence_mbar_init();
   mbar_wait(b, 0);
 }
+
+// Reads and clears the status word in one atomic exchange, so that a timeout
+// recorded by a kernel on another stream is either taken here or left for the
+// next read, never lost between a read and a separate clear.
+__global__ void status_take_kernel() { g_status_taken = atomicExch(&g_status, 0u); }
 
 // ---------------------------------------------------------------------- TMA
 // 3-D tiled load global -> shared, completion counted on `bar` in bytes.

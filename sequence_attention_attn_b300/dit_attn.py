@@ -215,12 +215,13 @@ def dit_attn_fwd_torus(q, k_src, v_src, k, v, partials, lses, out, lse_out, n_kv
 
 
 def cfg_combine_relmae(eps_c, eps_u, w: float, out, sums, stream=None) -> None:
-    """cfg_combine plus sums = [sum |eps_c - eps_u|, sum |eps_u|] (fp64 [2] on the
-    device); the rel-MAE discrepancy of the two guidance paths is sums[0] / sums[1]."""
+    """cfg_combine plus sums = [sum |eps_c - eps_u|, sum |eps_u|, rel-MAE] (fp64 [3]
+    on the device); the library computes the rel-MAE discrepancy of the two
+    guidance paths, sums[0] / sums[1], on the device."""
     _need(eps_c, "eps_c", torch.float32)
     _need(eps_u, "eps_u", torch.float32, eps_c.shape)
     _need(out, "out", torch.float32, eps_c.shape)
-    _need(sums, "sums", torch.float64, (2,))
+    _need(sums, "sums", torch.float64, (3,))
     rc = lib().cfg_combine_relmae(eps_c.data_ptr(), eps_u.data_ptr(), float(w), out.data_ptr(), eps_c.numel(),
                                   sums.data_ptr(), _stream(stream))
     _check(rc, "cfg_combine_relmae")
@@ -296,10 +297,9 @@ def attention_torus(q, k_src, v_src, n_kv_chunks: int, stream=None, copy_stream=
 
 
 def combine_relmae(eps_c, eps_u, w: float, stream=None):
-    """Returns (out, rel_mae) with rel_mae = sum |eps_c - eps_u| / sum |eps_u| as a
-    Python float (reading it waits for the stream)."""
+    """Returns (out, rel_mae): rel_mae = sum |eps_c - eps_u| / sum |eps_u| as the
+    library computed it, read back as a Python float (reading waits for the stream)."""
     out = torch.empty_like(eps_c)
-    sums = torch.empty(2, dtype=torch.float64, device=eps_c.device)
+    sums = torch.empty(3, dtype=torch.float64, device=eps_c.device)
     cfg_combine_relmae(eps_c, eps_u, w, out, sums, stream)
-    d, b = sums.tolist()
-    return out, d / b
+    return out, sums[2].item()

@@ -49,7 +49,7 @@ def test_library_exports_every_header_symbol(lib):
 
 
 def test_status_strings(lib):
-    assert lib.dit_abi_version() == 1
+    assert lib.dit_abi_version() == 2
     for code in range(-7, 1):
         s = dit_attn.status_string(code)
         assert s and s != "unknown status"
@@ -113,6 +113,7 @@ def test_cfg_relmae_rejects_bad_arguments_on_host(lib):
     assert f(A, B_, float("inf"), O, 100, S_, None) == INVALID
     assert f(A, B_, 4.5, O, 100, S_ + 4, None) == MISALIGNED        # sums not 8-byte aligned
     assert f(A, B_, 4.5, O, 100, A + 64, None) == INVALID           # sums inside eps_c
+    assert f(A, B_, 4.5, O, 100, O - 16, None) == INVALID           # sums[2] (the ratio) over out
     assert f(A, B_, 4.5, A + 16, 100, S_, None) == INVALID          # out partly over eps_c
 
 
@@ -166,4 +167,6 @@ def test_torus_rejects_bad_arguments_on_host(lib):
     assert call(k=V) == INVALID                   # k and v the same buffer
     assert call(p=A) == INVALID                   # partials over q
     assert call(ks=K) == INVALID                  # source is the landing buffer
+    assert call(ks=V) == INVALID                  # k_src is v: chunk copies into v overwrite it
+    assert call(vs=K + 64) == INVALID             # v_src overlaps k
     assert call(ls=P + 64) == INVALID             # lses inside partials

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle
-from parity_util import (check_attention, check_f32, f64, oracle_rows, sample_rows)
+from parity_util import (abs_weighted, check_attention, check_f32, f64, oracle_rows, sample_rows)
 from sequence_attention_attn_b300 import dit_attn, workloads
 
 pytestmark = pytest.mark.gpu
@@ -56,17 +56,19 @@ def test_cfg_combine_sizes_and_alias(numel):
 # ----------------------------------------------- CFG combine + rel-MAE
 def check_relmae(eps_c, eps_u, w, what):
     ref_out, (ref_d, ref_b) = oracle.cfg_relmae(eps_c.numpy(), eps_u.numpy(), w)
+    ref_ratio = oracle.cfg_relmae_ratio(eps_c.numpy(), eps_u.numpy())
     c, u = to_dev(eps_c, eps_u)
     out = torch.empty_like(c)
-    sums = torch.empty(2, dtype=torch.float64, device=DEV)
+    sums = torch.full((3,), float("nan"), dtype=torch.float64, device=DEV)
     dit_attn.cfg_combine_relmae(c, u, w, out, sums)
     check_f32(out, ref_out, f"{what} combine")
     # the fused combine is the plain combine, bit for bit
     assert torch.equal(out, dit_attn.combine(c, u, w)), what
-    d, b = sums.tolist()
+    d, b, ratio = sums.tolist()
     assert abs(d - ref_d) <= 1e-5 * ref_d + 1e-30, (what, d, ref_d)
     assert abs(b - ref_b) <= 1e-5 * ref_b, (what, b, ref_b)
-    assert abs(d / b - ref_d / ref_b) <= 1e-5 * (ref_d / ref_b) + 1e-30, what
+    # the ratio is computed on the device
+    assert abs(ratio - ref_ratio) <= 1e-5 * ref_ratio + 1e-30, (what, ratio, ref_ratio)
     assert_no_device_error()
 
 
@@ -89,9 +91,23 @@ def test_cfg_relmae_closed_forms_and_alias():
         cd, ud = to_dev(c, eps_u)
         out, rel = dit_attn.combine_relmae(cd, ud, 4.5)
         assert abs(rel - want) <= 1e-6, (want, rel)
+    # all-zero unconditional noise: identical paths give 0, any difference +inf
+    zero = torch.zeros(777, device=DEV)
+    assert dit_attn.combine_relmae(zero, zero, 4.5)[1] == 0.0
+    bump = zero.clone()
+    bump[500] = -0.25
+    assert dit_attn.combine_relmae(bump, zero, 4.5)[1] == float("inf")
+    # two calls in a row on one buffer: each starts from zero
+    c, u = to_dev(*workloads.make_cfg((1 << 16,), 9))
+    sums = torch.empty(3, dtype=torch.float64, device=DEV)
+    o = torch.empty_like(c)
+    dit_attn.cfg_combine_relmae(c, u, 4.5, o, sums)
+    first = sums.clone()
+    dit_attn.cfg_combine_relmae(c, u, 4.5, o, sums)
+    assert torch.allclose(first, sums, rtol=1e-12, atol=0.0)
     c, u = to_dev(*workloads.make_cfg((1000,), 6))
     ref = dit_attn.combine(c, u, 4.5)
-    sums = torch.empty(2, dtype=torch.float64, device=DEV)
+    sums = torch.empty(3, dtype=torch.float64, device=DEV)
     dit_attn.cfg_combine_relmae(c, u, 4.5, c, sums)       # in place over eps_c
     assert torch.equal(c, ref)
 
@@ -200,33 +216,57 @@ def test_attention_offsets_past_32_bits_sampled():
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("S", [1, 2, 100, 127, 128, 129, 255, 257, 383, 640])
+EDGE_S = [1, 2, 100, 127, 128, 129, 255, 257, 383, 640]
+
+
+def edge_chunk_counts(S):
+    return sorted({1, min(S, 3), min(S, 7), S if S <= 16 else 16})
+
+
+@pytest.mark.parametrize("S", EDGE_S)
 @pytest.mark.parametrize("D", [64, 72, 128])
 def test_attention_edge_lengths(S, D):
     q, k, v = workloads.make_random_qkv(1, 3, S, D, seed=S * 7 + D, std=1.5)
-    o_ref, l_ref = oracle.attention(f64(q), f64(k), f64(v))
-    for n in sorted({1, min(S, 3), min(S, 7), S if S <= 16 else 16}):
+    qf, kf, vf = f64(q), f64(k), f64(v)
+    o_ref, l_ref = oracle.attention(qf, kf, vf)
+    a_ref = abs_weighted(qf, kf, vf)
+    for n in edge_chunk_counts(S):
         out, lse = run_attention(q, k, v, n)
-        check_attention(out, lse, o_ref, l_ref, f"S={S} D={D} n={n}", scaled=True)
+        check_attention(out, lse, o_ref, l_ref, f"S={S} D={D} n={n}", abs_ref=a_ref)
+
+
+@pytest.mark.parametrize("S", EDGE_S)
+@pytest.mark.parametrize("D", [64, 72, 128])
+def test_attention_edge_lengths_unit_std(S, D):
+    # the same shapes with N(0, 1) inputs, held to the plain absolute bounds
+    q, k, v = workloads.make_random_qkv(1, 3, S, D, seed=S * 11 + D + 1, std=1.0)
+    o_ref, l_ref = oracle.attention(f64(q), f64(k), f64(v))
+    for n in edge_chunk_counts(S):
+        out, lse = run_attention(q, k, v, n)
+        check_attention(out, lse, o_ref, l_ref, f"std 1 S={S} D={D} n={n}")
 
 
 def test_attention_chunks_shorter_than_a_tile():
     # 40 chunks of 6-7 keys: every tile is cut at a chunk end
     q, k, v = workloads.make_random_qkv(2, 2, 260, 64, seed=99, std=2.0)
-    o_ref, l_ref = oracle.attention(f64(q), f64(k), f64(v))
+    qf, kf, vf = f64(q), f64(k), f64(v)
+    o_ref, l_ref = oracle.attention(qf, kf, vf)
+    a_ref = abs_weighted(qf, kf, vf)
     out, lse = run_attention(q, k, v, 40)
-    check_attention(out, lse, o_ref, l_ref, "n=40", scaled=True)
+    check_attention(out, lse, o_ref, l_ref, "n=40", abs_ref=a_ref)
     out, lse = run_attention(q, k, v, 260)   # one key per chunk
-    check_attention(out, lse, o_ref, l_ref, "n=S", scaled=True)
+    check_attention(out, lse, o_ref, l_ref, "n=S", abs_ref=a_ref)
 
 
 def test_attention_sharp_softmax():
     # large logits: the reference max moves often and by a lot
     q, k, v = workloads.make_random_qkv(1, 4, 512, 128, seed=5, std=4.0)
-    o_ref, l_ref = oracle.attention(f64(q), f64(k), f64(v))
+    qf, kf, vf = f64(q), f64(k), f64(v)
+    o_ref, l_ref = oracle.attention(qf, kf, vf)
+    a_ref = abs_weighted(qf, kf, vf)
     for n in (1, 3):
         out, lse = run_attention(q, k, v, n)
-        check_attention(out, lse, o_ref, l_ref, f"sharp n={n}", scaled=True)
+        check_attention(out, lse, o_ref, l_ref, f"sharp n={n}", abs_ref=a_ref)
 
 
 def test_attention_without_lse_output():

@@ -13,7 +13,7 @@ import torch
 from hypothesis import HealthCheck, given, settings, strategies as st
 
 import oracle
-from parity_util import check_attention, check_f32, f64
+from parity_util import abs_weighted, check_attention, check_f32, f64
 from sequence_attention_attn_b300 import dit_attn, workloads
 
 pytestmark = pytest.mark.gpu
@@ -40,12 +40,14 @@ def attn_case(draw):
 def test_attention_random_shapes(case):
     B, H, S, D, n, std, seed = case
     q, k, v = workloads.make_random_qkv(B, H, S, D, seed=seed, std=std)
-    o_ref, l_ref = oracle.attention(f64(q), f64(k), f64(v))
+    qf, kf, vf = f64(q), f64(k), f64(v)
+    o_ref, l_ref = oracle.attention(qf, kf, vf)
     qd, kd, vd = (t.to(DEV) for t in (q, k, v))
     out, lse = dit_attn.attention(qd, kd, vd, n_kv_chunks=n)
     torch.cuda.synchronize()
     assert dit_attn.dit_last_device_status() == 0
-    check_attention(out, lse, o_ref, l_ref, f"B={B} H={H} S={S} D={D} n={n} std={std}", scaled=True)
+    check_attention(out, lse, o_ref, l_ref, f"B={B} H={H} S={S} D={D} n={n} std={std}",
+                    abs_ref=abs_weighted(qf, kf, vf))
 
 
 @SETTINGS
@@ -61,7 +63,7 @@ def test_partials_random_shapes(case):
     for c, (j0, j1) in enumerate(oracle.chunk_bounds(S, n)):
         o_c, l_c = oracle.attention(qf, kf, vf, j0, j1)
         check_attention(parts[c], lses[c], o_c.reshape(-1, D), l_c.reshape(-1), f"S={S} D={D} chunk {c}/{n}",
-                        scaled=True)
+                        abs_ref=abs_weighted(qf, kf, vf, j0, j1).reshape(-1, D))
 
 
 @SETTINGS
@@ -99,13 +101,15 @@ def range_case(draw):
 def test_key_range_random(case):
     B, H, S, D, j0, j1, std, seed = case
     q, k, v = workloads.make_random_qkv(B, H, S, D, seed=seed, std=std)
-    o_ref, l_ref = oracle.attention(f64(q), f64(k), f64(v), j0, j1)
+    qf, kf, vf = f64(q), f64(k), f64(v)
+    o_ref, l_ref = oracle.attention(qf, kf, vf, j0, j1)
     qd, kd, vd = (t.to(DEV) for t in (q, k, v))
     out, lse = dit_attn.attention_range(qd, kd, vd, j0, j1)
     torch.cuda.synchronize()
     assert dit_attn.dit_last_device_status() == 0
     check_attention(out, lse, o_ref.reshape(-1, D), l_ref.reshape(-1),
-                    f"B={B} H={H} S={S} D={D} [{j0},{j1}) std={std}", scaled=True)
+                    f"B={B} H={H} S={S} D={D} [{j0},{j1}) std={std}",
+                    abs_ref=abs_weighted(qf, kf, vf, j0, j1).reshape(-1, D))
 
 
 @settings(max_examples=15, deadline=None, derandomize=True, database=None,
@@ -114,10 +118,12 @@ def test_key_range_random(case):
 def test_torus_random(case):
     B, H, S, D, n, std, seed = case
     q, k, v = workloads.make_random_qkv(B, H, S, D, seed=seed, std=std)
-    o_ref, l_ref = oracle.attention(f64(q), f64(k), f64(v))
+    qf, kf, vf = f64(q), f64(k), f64(v)
+    o_ref, l_ref = oracle.attention(qf, kf, vf)
     out, lse = dit_attn.attention_torus(q.to(DEV), k.pin_memory(), v.pin_memory(), n,
                                         copy_stream=torch.cuda.Stream())
     torch.cuda.synchronize()
     assert dit_attn.dit_last_device_status() == 0
     check_attention(out, lse, o_ref.reshape(-1, D), l_ref.reshape(-1),
-                    f"torus B={B} H={H} S={S} D={D} n={n} std={std}", scaled=True)
+                    f"torus B={B} H={H} S={S} D={D} n={n} std={std}",
+                    abs_ref=abs_weighted(qf, kf, vf).reshape(-1, D))

@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle
-from parity_util import check_attention, f64, oracle_rows, sample_rows
+from parity_util import abs_weighted, check_attention, f64, oracle_rows, sample_rows
 from sequence_attention_attn_b300 import dit_attn, workloads
 
 pytestmark = pytest.mark.gpu
@@ -37,7 +37,7 @@ def test_range_matches_oracle(S, D):
         assert_no_device_error()
         o_ref, l_ref = oracle.attention(qf, kf, vf, j0, j1)
         check_attention(out, lse, o_ref.reshape(-1, D), l_ref.reshape(-1), f"S={S} D={D} [{j0},{j1})",
-                        scaled=True)
+                        abs_ref=abs_weighted(qf, kf, vf, j0, j1).reshape(-1, D))
 
 
 def test_range_ignores_keys_outside_the_range():
@@ -53,6 +53,26 @@ def test_range_ignores_keys_outside_the_range():
         t[:, :, j1:] = -3.0
     out_b, lse_b = dit_attn.attention_range(q, k2, v2, j0, j1)
     assert torch.equal(out_a, out_b) and torch.equal(lse_a, lse_b)
+
+
+@pytest.mark.parametrize("D", [64, 72, 128])
+def test_range_reads_no_key_row_outside_the_range(D):
+    # Every key and value row outside [j0, j1) is NaN: the range kernel must
+    # read none of them (the last tile's tail past j1 is zero-filled, not read).
+    S = 700
+    q, k, v = workloads.make_random_qkv(1, 3, S, D, seed=40 + D)
+    qf, kf, vf = f64(q), f64(k), f64(v)
+    qd = q.to(DEV)
+    for j0, j1 in ((130, 300), (0, 5), (127, 129), (600, 700), (0, 700)):
+        kd, vd = k.to(DEV), v.to(DEV)
+        for t in (kd, vd):
+            t[:, :, :j0] = float("nan")
+            t[:, :, j1:] = float("nan")
+        out, lse = dit_attn.attention_range(qd, kd, vd, j0, j1)
+        torch.cuda.synchronize()
+        assert_no_device_error()
+        o_ref, l_ref = oracle.attention(qf, kf, vf, j0, j1)
+        check_attention(out, lse, o_ref.reshape(-1, D), l_ref.reshape(-1), f"NaN outside [{j0},{j1}) D={D}")
 
 
 def test_ranges_merge_to_full_attention():
@@ -103,10 +123,11 @@ def test_torus_equals_partials_then_merge_bitwise():
         assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse), n
 
 
-def test_torus_waits_for_every_row_its_tiles_read():
+def test_torus_reads_only_landed_rows():
     # The landing buffers start as NaN.  Chunks of 40 keys end inside a
-    # 128-key tile, so chunk c's last tile reads (masked) rows of later chunks;
-    # computing before those rows have landed would turn the output into NaN.
+    # 128-key tile and chunk c is computed as soon as its own rows have
+    # landed, while later chunks' rows may still be NaN: the result must not
+    # depend on them.
     S, D, n = 1000, 64, 25
     q, k, v = workloads.make_random_qkv(1, 4, S, D, seed=12)
     qd = q.to(DEV)
@@ -150,3 +171,13 @@ def test_torus_argument_checks_in_binding():
         dit_attn.attention_torus(q, pageable, pageable, 2)
     with pytest.raises(dit_attn.DitError):
         dit_attn.attention_torus(q, q.clone(), q.clone(), 65)
+    # a source that is the other landing buffer is rejected before any copy
+    k, v = torch.empty_like(q), torch.empty_like(q)
+    rows = 128
+    parts = torch.empty((2, rows, 64), dtype=torch.float32, device=DEV)
+    lses = torch.empty((2, rows), dtype=torch.float32, device=DEV)
+    out = torch.empty((rows, 64), dtype=torch.float32, device=DEV)
+    with pytest.raises(dit_attn.DitError):
+        dit_attn.dit_attn_fwd_torus(q, v, q.clone(), k, v, parts, lses, out, None, 2)
+    with pytest.raises(dit_attn.DitError):
+        dit_attn.dit_attn_fwd_torus(q, q.clone(), k, k, v, parts, lses, out, None, 2)
