@@ -117,37 +117,46 @@ struct AttnParams {
   int num_pairs;       // ceil(ceil(S / 128) / 2)
   int tiles_total;     // merged mode: number of key tiles over all chunks
   int key_j0, key_j1;  // partials mode with key_j1 > 0: one key range, written to slot 0
+  int chunk_q, chunk_r;  // S = chunk_q * n_chunks + chunk_r (merged mode's chunk walk)
   float scale_log2;    // log2(e) / sqrt(D)
 };
 
-// Walks the key tiles chunk by chunk.
+// Walks the key tiles chunk by chunk: every chunk starts a new tile and a
+// tile stops at its chunk's end (columns past it are masked).  Chunk c covers
+// [floor(c S / n), floor((c + 1) S / n)); the chunk ends are stepped without
+// a division: with S = q n + r, chunk c ends q keys after the previous end,
+// plus one when the running remainder (c + 1) r mod n wraps past n.  q, r and
+// n stay in the kernel parameters; a single key range is one chunk.
 struct KvIter {
-  int S, n, c, j0, j1, t0;
-  __device__ __forceinline__ void start(int S_, int n_, int c_) {
-    S = S_;
-    n = n_;
-    c = c_;
-    j0 = static_cast<int>((static_cast<long long>(c) * S) / n);
-    j1 = static_cast<int>((static_cast<long long>(c + 1) * S) / n);
-    t0 = j0;
+  int j0, j1;  // current chunk [j0, j1)
+  int t0;      // first key of the current tile
+  int rem;     // (c + 1) r mod n for the current chunk c
+  __device__ __forceinline__ void start(int q, int r) {
+    j0 = 0;
+    j1 = q;
+    t0 = 0;
+    rem = r;
   }
-  // A single explicit key range [j0_, j1_) (one chunk).
+  // A single explicit key range [j0_, j1_).
   __device__ __forceinline__ void start_range(int j0_, int j1_) {
-    S = j1_;
-    n = 1;
-    c = 0;
     j0 = j0_;
     j1 = j1_;
     t0 = j0_;
+    rem = 0;
   }
   __device__ __forceinline__ int valid() const { return min(kBlockN, j1 - t0); }
   __device__ __forceinline__ bool chunk_start() const { return t0 == j0; }
-  __device__ __forceinline__ void next() {
+  // q, r, n: the partition (S = q n + r); unused once the last chunk is done.
+  __device__ __forceinline__ void next(int q, int r, int n) {
     t0 += kBlockN;
     if (t0 >= j1) {
-      ++c;
       j0 = j1;
-      j1 = static_cast<int>((static_cast<long long>(c + 1) * S) / n);
+      j1 += q;
+      rem += r;
+      if (rem >= n) {
+        rem -= n;
+        ++j1;
+      }
       t0 = j0;
     }
   }
@@ -261,8 +270,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Work unit.
+  // Work unit and its key walk.
   int bh, pair, chunk_first, tiles;
+  KvIter kv0;
   if constexpr (kPartials) {
     const int per_bh_chunk = p.num_pairs;
     const int u = blockIdx.x;
@@ -273,11 +283,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const long long j0 = p.key_j1 > 0 ? p.key_j0 : (static_cast<long long>(chunk_first) * p.S) / p.n_chunks;
     const long long j1 = p.key_j1 > 0 ? p.key_j1 : (static_cast<long long>(chunk_first + 1) * p.S) / p.n_chunks;
     tiles = static_cast<int>((j1 - j0 + kBlockN - 1) / kBlockN);
+    kv0.start_range(static_cast<int>(j0), static_cast<int>(j1));
   } else {
     pair = blockIdx.x % p.num_pairs;
     bh = blockIdx.x / p.num_pairs;
     chunk_first = 0;
     tiles = p.tiles_total;
+    kv0.start(p.chunk_q, p.chunk_r);
   }
   const int q_row0 = pair * 2 * kBlockM;
   const bool has1 = q_row0 + kBlockM < p.S;
@@ -357,9 +369,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if constexpr (C::kTail > 0)
           tma_load_3d(dst + kSwzBytes, &tm_q_tail, q_full(t), 64, q_row0 + t * kBlockM, bh, pol_q);
       }
-      KvIter kv;
-      if (kPartials && p.key_j1 > 0) kv.start_range(p.key_j0, p.key_j1);
-      else kv.start(p.S, p.n_chunks, chunk_first);
+      KvIter kv = kv0;
       int k_last[NS], v_last[NS];  // last use issued on each stage, -1 if none
 #pragma unroll
       for (int s = 0; s < NS; ++s) k_last[s] = v_last[s] = -1;
@@ -378,7 +388,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tma_load_3d(vd, &tm_v, v_full(s), 0, kv.t0, bh, pol_kv);
         if constexpr (C::kVTail > 0) tma_load_3d(vd + kSwzBytes, &tm_v_tail, v_full(s), 64, kv.t0, bh, pol_kv);
         v_last[s] = u;
-        kv.next();
+        kv.next(p.chunk_q, p.chunk_r, p.n_chunks);
       }
       // Drain: every load issued must land before the CTA may exit.  Waiting on
       // the parity of a stage's last use returns at once if it already landed.
@@ -494,9 +504,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       float m = -INFINITY;     // reference max, base-2 scaled units
       float l = 0.0f;          // row sum of the current chunk
       float l_run = -INFINITY; // merged log2-LSE of finished chunks
-      KvIter kv;
-      if (kPartials && p.key_j1 > 0) kv.start_range(p.key_j0, p.key_j1);
-      else kv.start(p.S, p.n_chunks, chunk_first);
+      KvIter kv = kv0;
       bool ok = true;
       for (int it = 0; it < tiles; ++it) {
         if (!(ok = mbar_wait_warp(s_full(t), it & 1))) break;
@@ -535,7 +543,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           // The previous chunk is complete: fold its LSE into the running one.
           // Its partial output is already in the accumulator with the shared
           // reference m, so the O half of the merge is applied at the end.
-          l_run = logaddexp2(l_run, m + lg2_approx(l));
+          l_run = logaddexp2(l_run, m + lg2_approx(fmaxf(l, 0.0f)));
           l = 0.0f;
         }
         if (tmax > m + kRescaleThreshold) {
@@ -581,12 +589,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(p_full(t));
-        kv.next();
+        kv.next(p.chunk_q, p.chunk_r, p.n_chunks);
       }
       if (ok) ok = mbar_wait_warp(o_full(t), 0);
       if (ok) {
         tc_fence_after();
-        const float lse_c = m + lg2_approx(l);
+        const float lse_c = m + lg2_approx(fmaxf(l, 0.0f));
         const float l_new = logaddexp2(l_run, lse_c);
         const float sc = ex2_approx(m - l_new);
         const int row = q_row0 + t * kBlockM + row_in_tile;

@@ -200,6 +200,8 @@ dit_status attn_dispatch(const void *q, const void *k, const void *v, void *out,
   prm.tiles_total = static_cast<int>(tiles_total);
   prm.key_j0 = key_j0;
   prm.key_j1 = key_j1;
+  prm.chunk_q = S / n;
+  prm.chunk_r = S % n;
   prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   switch (D) {
