@@ -250,7 +250,12 @@ __device__ __forceinline__ void store_f32_row(float *dst, const uint32_t *r, int
 // ------------------------------------------------------------------ kernel
 // kPartials = false: all chunks, merged on chip, bf16 O + fp32 LSE.
 // kPartials = true : one chunk per CTA, fp32 O_c + LSE_c, no merge.
-template <int D, bool kPartials>
+// kPdl: launched with programmatic stream serialization (see ptx.cuh); the
+//   host takes it for grids of a few waves, where the launch gap between
+//   kernels is a visible share of the time.  Long grids use the plain launch
+//   and a kernel without the two grid-dependency instructions, whose position
+//   in the code measurably cost the D = 64 loop about 2 %.
+template <int D, bool kPartials, bool kPdl>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_q_tail,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_k_tail,
@@ -355,6 +360,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+  if constexpr (kPdl) {
+    // The next kernel in the stream may launch now: its CTAs take the SMs
+    // this grid leaves idle or frees, run their prologue and wait here.
+    // Every global read and write of this grid comes after the wait for the
+    // previous kernel to have completed.
+    griddep_launch_dependents();
+    griddep_wait();
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer

@@ -14,6 +14,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <utility>
 
 #include "dit_attn.h"
 #include "attn_fwd.cuh"
@@ -41,7 +42,7 @@ struct DeviceState {
   // Events of the Torus pipeline (created on first use, reused by every call).
   cudaEvent_t torus_events[kMaxTorusChunks + 1] = {};
   bool torus_events_ready = false;
-  bool attr_set[3][2] = {};  // per head-dim instantiation x partials
+  bool attr_set[3][2][2] = {};  // per head-dim instantiation x partials x programmatic launch
 };
 
 std::mutex g_mu;
@@ -114,6 +115,25 @@ dit_status encode_qkv_map(CUtensorMap *map, const void *ptr, long long BH, int S
   return r == CUDA_SUCCESS ? DIT_OK : DIT_ERR_CUDA;
 }
 
+// Launches a kernel with programmatic stream serialization: it may start
+// while the previous kernel in the stream finishes, and waits for it (in the
+// kernel, griddep_wait) before touching memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 int head_dim_index(int D) { return D == 64 ? 0 : (D == 72 ? 1 : (D == 128 ? 2 : -1)); }
 
 dit_status check_attn_args(const void *q, const void *k, const void *v, int B, int H, int S, int D, int n) {
@@ -125,18 +145,24 @@ dit_status check_attn_args(const void *q, const void *k, const void *v, int B, i
   return DIT_OK;
 }
 
+// Grids of up to this many waves (one CTA per SM) take the programmatic
+// launch: the next kernel's CTAs start on the SMs this one leaves idle.
+constexpr int kPdlMaxWaves = 8;
+
 template <int D, bool kPartials>
 dit_status launch_attn(DeviceState &st, int didx, const void *q, const void *k, const void *v,
                        const ditk::AttnParams &prm, long long BH, int S, int grid, cudaStream_t stream) {
   using L = ditk::AttnLayout<D>;
-  auto kernel = ditk::attn_fwd_kernel<D, kPartials>;
+  const bool pdl = grid <= kPdlMaxWaves * st.sm_count;
+  auto kernel = pdl ? ditk::attn_fwd_kernel<D, kPartials, true> : ditk::attn_fwd_kernel<D, kPartials, false>;
   {
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!st.attr_set[didx][kPartials ? 1 : 0]) {
+    bool &done = st.attr_set[didx][kPartials ? 1 : 0][pdl ? 1 : 0];
+    if (!done) {
       if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemLaunch) !=
           cudaSuccess)
         return DIT_ERR_CUDA;
-      st.attr_set[didx][kPartials ? 1 : 0] = true;
+      done = true;
     }
   }
   CUtensorMap mq, mq_t, mk, mk_t, mv, mv_t;
@@ -159,7 +185,13 @@ dit_status launch_attn(DeviceState &st, int didx, const void *q, const void *k, 
     mk_t = mk;
   }
   mv_t = mv;
-  kernel<<<grid, ditk::kAttnThreads, L::kSmemLaunch, stream>>>(mq, mq_t, mk, mk_t, mv, mv_t, prm);
+  if (pdl) {
+    if (launch_pdl(kernel, dim3(grid), dim3(ditk::kAttnThreads), L::kSmemLaunch, stream, mq, mq_t, mk, mk_t, mv,
+                   mv_t, prm) != cudaSuccess)
+      return DIT_ERR_LAUNCH;
+  } else {
+    kernel<<<grid, ditk::kAttnThreads, L::kSmemLaunch, stream>>>(mq, mq_t, mk, mk_t, mv, mv_t, prm);
+  }
   return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ERR_LAUNCH;
 }
 
@@ -403,11 +435,13 @@ dit_status dit_attn_merge(const float *partials, const float *lses, int n, float
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (D % 4 == 0) {
     const int d4 = D / 4;
-    ditk::lse_merge_vec4_kernel<<<stream_grid(*st, rows * d4), ditk::kStreamThreads, 0, cs>>>(
-        partials, lses, n, out, lse_out, rows, d4);
+    if (launch_pdl(ditk::lse_merge_vec4_kernel, dim3(stream_grid(*st, rows * d4)), dim3(ditk::kStreamThreads), 0, cs,
+                   partials, lses, n, out, lse_out, rows, d4) != cudaSuccess)
+      return DIT_ERR_LAUNCH;
   } else {
-    ditk::lse_merge_scalar_kernel<<<stream_grid(*st, rows * D), ditk::kStreamThreads, 0, cs>>>(
-        partials, lses, n, out, lse_out, rows, D);
+    if (launch_pdl(ditk::lse_merge_scalar_kernel, dim3(stream_grid(*st, rows * D)), dim3(ditk::kStreamThreads), 0, cs,
+                   partials, lses, n, out, lse_out, rows, D) != cudaSuccess)
+      return DIT_ERR_LAUNCH;
   }
   return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ERR_LAUNCH;
 }
@@ -430,12 +464,15 @@ dit_status cfg_combine(const float *eps_c, const float *eps_u, float w, float *o
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const long long n4 = numel / 4;
   if (n4 > 0) {
-    ditk::cfg_combine_vec4_kernel<<<stream_grid(*st, n4), ditk::kStreamThreads, 0, cs>>>(
-        reinterpret_cast<const float4 *>(eps_c), reinterpret_cast<const float4 *>(eps_u), w,
-        reinterpret_cast<float4 *>(out), n4);
+    if (launch_pdl(ditk::cfg_combine_vec4_kernel, dim3(stream_grid(*st, n4)), dim3(ditk::kStreamThreads), 0, cs,
+                   reinterpret_cast<const float4 *>(eps_c), reinterpret_cast<const float4 *>(eps_u), w,
+                   reinterpret_cast<float4 *>(out), n4) != cudaSuccess)
+      return DIT_ERR_LAUNCH;
   }
   if (numel % 4 != 0) {
-    ditk::cfg_combine_tail_kernel<<<1, 32, 0, cs>>>(eps_c, eps_u, w, out, n4 * 4, numel);
+    if (launch_pdl(ditk::cfg_combine_tail_kernel, dim3(1), dim3(32), 0, cs, eps_c, eps_u, w, out, n4 * 4, numel) !=
+        cudaSuccess)
+      return DIT_ERR_LAUNCH;
   }
   return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ERR_LAUNCH;
 }
@@ -461,7 +498,9 @@ dit_status cfg_combine_relmae(const float *eps_c, const float *eps_u, float w, f
   if (cudaMemsetAsync(sums, 0, 3 * sizeof(double), cs) != cudaSuccess) return DIT_ERR_CUDA;
   const long long n4 = numel / 4;
   const int grid = stream_grid(*st, n4 > 0 ? n4 : 1);
-  ditk::cfg_combine_relmae_kernel<<<grid, ditk::kStreamThreads, 0, cs>>>(eps_c, eps_u, w, out, numel, sums);
+  if (launch_pdl(ditk::cfg_combine_relmae_kernel, dim3(grid), dim3(ditk::kStreamThreads), 0, cs, eps_c, eps_u, w, out,
+                 numel, sums) != cudaSuccess)
+    return DIT_ERR_LAUNCH;
   return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ERR_LAUNCH;
 }
 

@@ -17,7 +17,9 @@
 // Both are pure streams: each output element is written once and each input
 // element read once, 16 bytes per thread access, consecutive threads on
 // consecutive addresses.  Grids are a multiple of the SM count with a
-// grid-stride loop.
+// grid-stride loop.  Each kernel lets the next one in the stream launch at
+// once and waits for the previous one before its first memory access
+// (programmatic dependent launch, see ptx.cuh).
 #pragma once
 #include <cstdint>
 
@@ -48,6 +50,8 @@ __device__ __forceinline__ float merged_lse(const float *__restrict__ lses, int 
 __global__ void __launch_bounds__(kStreamThreads)
     lse_merge_vec4_kernel(const float *__restrict__ partials, const float *__restrict__ lses, int n,
                           float *__restrict__ out, float *__restrict__ lse_out, long long rows, int d4) {
+  griddep_launch_dependents();
+  griddep_wait();
   const long long total = rows * d4;
   const long long stride = static_cast<long long>(gridDim.x) * kStreamThreads;
   for (long long idx = static_cast<long long>(blockIdx.x) * kStreamThreads + threadIdx.x; idx < total;
@@ -84,6 +88,8 @@ __global__ void __launch_bounds__(kStreamThreads)
 __global__ void __launch_bounds__(kStreamThreads)
     lse_merge_scalar_kernel(const float *__restrict__ partials, const float *__restrict__ lses, int n,
                             float *__restrict__ out, float *__restrict__ lse_out, long long rows, int D) {
+  griddep_launch_dependents();
+  griddep_wait();
   const long long total = rows * D;
   const long long stride = static_cast<long long>(gridDim.x) * kStreamThreads;
   for (long long idx = static_cast<long long>(blockIdx.x) * kStreamThreads + threadIdx.x; idx < total;
@@ -109,6 +115,8 @@ __global__ void __launch_bounds__(kStreamThreads)
 // the same thread, so no __restrict__ here.
 __global__ void __launch_bounds__(kStreamThreads)
     cfg_combine_vec4_kernel(const float4 *eps_c, const float4 *eps_u, float w, float4 *out, long long n4) {
+  griddep_launch_dependents();
+  griddep_wait();
   const long long stride = static_cast<long long>(gridDim.x) * kStreamThreads;
   for (long long i = static_cast<long long>(blockIdx.x) * kStreamThreads + threadIdx.x; i < n4; i += stride) {
     const float4 c = ld_stream(eps_c + i);
@@ -170,6 +178,8 @@ __device__ __forceinline__ void block_add_sums(double diff, double base, double 
 __global__ void __launch_bounds__(kStreamThreads)
     cfg_combine_relmae_kernel(const float *eps_c, const float *eps_u, float w, float *out, long long numel,
                               double *sums) {
+  griddep_launch_dependents();
+  griddep_wait();
   const long long n4 = numel >> 2;
   const float4 *c4 = reinterpret_cast<const float4 *>(eps_c);
   const float4 *u4 = reinterpret_cast<const float4 *>(eps_u);
@@ -213,6 +223,8 @@ __global__ void __launch_bounds__(kStreamThreads)
 
 __global__ void cfg_combine_tail_kernel(const float *eps_c, const float *eps_u, float w, float *out,
                                         long long begin, long long numel) {
+  griddep_launch_dependents();
+  griddep_wait();
   const long long i = begin + threadIdx.x;
   if (i < numel) out[i] = fmaf(w, eps_c[i] - eps_u[i], eps_u[i]);
 }

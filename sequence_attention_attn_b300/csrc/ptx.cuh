@@ -120,6 +120,17 @@ __global__ void selftest_wait_kernel() {
 // next read, never lost between a read and a separate clear.
 __global__ void status_take_kernel() { g_status_taken = atomicExch(&g_status, 0u); }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the previous kernel in the stream is still
+// running: launch_dependents lets the next kernel launch once every CTA of
+// this grid has issued it (or exited), and wait blocks until the previous
+// grid has completed and its memory operations are visible.  Without the
+// launch attribute both are no-ops.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------------- TMA
 // 3-D tiled load global -> shared, completion counted on `bar` in bytes.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
