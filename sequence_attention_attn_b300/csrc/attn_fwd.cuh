@@ -118,6 +118,8 @@ struct AttnParams {
   int tiles_total;     // merged mode: number of key tiles over all chunks
   int key_j0, key_j1;  // partials mode with key_j1 > 0: one key range, written to slot 0
   int chunk_q, chunk_r;  // S = chunk_q * n_chunks + chunk_r (merged mode's chunk walk)
+  int pair_units;      // merged mode: CTAs below this index take a pair of query tiles; each
+                       // later pair is split into two CTAs of one query tile (the last wave)
   float scale_log2;    // log2(e) / sqrt(D)
 };
 
@@ -278,6 +280,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   // Work unit and its key walk.
   int bh, pair, chunk_first, tiles;
   KvIter kv0;
+  int q_tile_in_pair = 0;
+  bool single = false;
   if constexpr (kPartials) {
     const int per_bh_chunk = p.num_pairs;
     const int u = blockIdx.x;
@@ -290,14 +294,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tiles = static_cast<int>((j1 - j0 + kBlockN - 1) / kBlockN);
     kv0.start_range(static_cast<int>(j0), static_cast<int>(j1));
   } else {
-    pair = blockIdx.x % p.num_pairs;
-    bh = blockIdx.x / p.num_pairs;
+    int g = blockIdx.x;
+    if (g >= p.pair_units) {
+      const int u = g - p.pair_units;
+      g = p.pair_units + (u >> 1);
+      q_tile_in_pair = u & 1;
+      single = true;
+    }
+    pair = g % p.num_pairs;
+    bh = g / p.num_pairs;
     chunk_first = 0;
     tiles = p.tiles_total;
     kv0.start(p.chunk_q, p.chunk_r);
   }
-  const int q_row0 = pair * 2 * kBlockM;
-  const bool has1 = q_row0 + kBlockM < p.S;
+  const int q_row0 = (pair * 2 + q_tile_in_pair) * kBlockM;
+  const bool has1 = !single && q_row0 + kBlockM < p.S;
 
   // Shared-memory addresses.
   const uint32_t sQ0 = base + L::kQOff;

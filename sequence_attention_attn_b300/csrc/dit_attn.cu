@@ -206,6 +206,7 @@ dit_status attn_dispatch(const void *q, const void *k, const void *v, void *out,
   const int num_pairs = (tiles_q + 1) / 2;
   long long grid = BH * num_pairs * (kPartials ? n : 1);
   if (grid > 2147483647LL) return DIT_ERR_INVALID_ARG;
+  long long pair_units = grid;
   // Key tiles over all chunks (each chunk starts a new tile).
   long long tiles_total = 0;
   for (int c = 0; c < n; ++c) {
@@ -219,6 +220,15 @@ dit_status attn_dispatch(const void *q, const void *k, const void *v, void *out,
   dit_status s = select_device(stream, &dev, &st);
   if (s != DIT_OK) return s;
   if ((s = get_encoder()) != DIT_OK) return s;
+  if (!kPartials) {
+    // A last wave of at most half the SMs: its pairs run as two single-tile
+    // CTAs each, on twice as many SMs.
+    const long long rem = grid % st->sm_count;
+    if (grid > st->sm_count && rem > 0 && 2 * rem <= st->sm_count) {
+      pair_units = grid - rem;
+      grid += rem;
+    }
+  }
 
   ditk::AttnParams prm{};
   prm.out = static_cast<__nv_bfloat16 *>(out);
@@ -232,6 +242,7 @@ dit_status attn_dispatch(const void *q, const void *k, const void *v, void *out,
   prm.tiles_total = static_cast<int>(tiles_total);
   prm.key_j0 = key_j0;
   prm.key_j1 = key_j1;
+  prm.pair_units = static_cast<int>(pair_units);
   prm.chunk_q = S / n;
   prm.chunk_r = S % n;
   prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
