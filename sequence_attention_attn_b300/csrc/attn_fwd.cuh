@@ -27,9 +27,11 @@
 // TMEM columns: S_t at 128 t.  D = 64: O_t at 256 + 64 t and P_t at
 // 384 + 64 t, so S_t of the next key tile is computed as soon as the softmax
 // has loaded S_t into registers (QK^T runs while the softmax works) and only
-// the PV that reads P_t has to wait for it.  D = 72, 128: no room for P on
-// its own; O_t at 256 + 128 t and P_t over the first 64 columns of S_t, so
-// QK^T of the next tile follows the PV of this one.
+// the PV that reads P_t has to wait for it.  D = 72: room for the P columns
+// of one query tile: O_0 at 256, O_1 at 352, P_0 at 448; tile 1 writes P_1
+// over the first 64 columns of S_1, so its QK^T of the next key tile follows
+// its PV of this one.  D = 128: no room for P on its own; O_t at 256 + 128 t
+// and P_t over the first 64 columns of S_t.
 // The two softmax groups ping-pong: while one group works on its tile the
 // tensor core runs the other tile's MMAs.
 //
@@ -328,8 +330,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   auto o_upd = [&](int t) { return bars + 8u * (11 + 4 * NS + t); };
   // s_free(t): the softmax group has loaded S_t (D = 64 only); o_upd(t): the
   // PV of tile t has completed, so P_t and O_t are free (D = 64 only).
-  constexpr bool kSplitP = (D == 64);
-  constexpr uint32_t kOStride = kSplitP ? 64u : 128u;
+  constexpr bool kSplitP = (D == 64);               // both query tiles
+  constexpr bool kSplitP0 = (D == 64 || D == 72);   // query tile 0
+  // TMEM columns of O_1, P_0, P_1 (O_0 at 256, S_t at 128 t).  D = 72 has room
+  // for P columns of one query tile only: O_0 [256, 336), O_1 [352, 432),
+  // P_0 [448, 512); P_1 is written over the first 64 columns of S_1.
+  constexpr uint32_t kO1 = D == 64 ? 320u : (D == 72 ? 352u : 384u);
+  constexpr uint32_t kP0 = D == 64 ? 384u : 448u;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kTmemSlotOff);
 
   if (threadIdx.x == 0) {
@@ -431,8 +438,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // The whole warp runs the loop; one elected lane issues each instruction.
     {
       const uint32_t tS0 = tmem_base, tS1 = tmem_base + 128;
-      const uint32_t tO0 = tmem_base + 256, tO1 = tmem_base + 256 + kOStride;
-      const uint32_t tP0 = kSplitP ? tmem_base + 384 : tS0, tP1 = kSplitP ? tmem_base + 448 : tS1;
+      const uint32_t tO0 = tmem_base + 256, tO1 = tmem_base + kO1;
+      const uint32_t tP0 = kSplitP0 ? tmem_base + kP0 : tS0, tP1 = kSplitP ? tmem_base + 448 : tS1;
       const uint32_t q_lo0 = desc_lo(sQ0, 16), k_lo0 = desc_lo(sK0, 16), v_lo0 = desc_lo(sV0, kSwzBytes);
       bool ok = mbar_wait_warp(q_full(0), 0) && (!has1 || mbar_wait_warp(q_full(1), 0));
       tc_fence_after();
@@ -472,6 +479,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
           umma_commit_e(k_empty(s));
           if (it > 0) umma_commit_e(v_empty(ps));
+        } else if constexpr (kSplitP0) {
+          // Query tile 0 as above; tile 1 writes P over S, so its QK^T of
+          // this key tile follows the PV of the previous one.
+          if (it > 0 && !(ok = mbar_wait_warp(s_free(0), (it - 1) & 1))) break;
+          tc_fence_after();
+          issue_qk<D>(tS0, q_lo0, ks);
+          umma_commit_e(s_full(0));
+          if (it > 0) {
+            if (!(ok = mbar_wait_warp(p_full(0), (it - 1) & 1))) break;
+            if (!(ok = mbar_wait_warp(v_full(ps), ((it - 1) / NS) & 1))) break;
+            tc_fence_after();
+            issue_pv<D>(tO0, tP0, vs, it > 1);
+            umma_commit_e(o_upd(0));
+          }
+          if (has1) {
+            if (it > 0) {
+              if (!(ok = mbar_wait_warp(p_full(1), (it - 1) & 1))) break;
+              tc_fence_after();
+              issue_pv<D>(tO1, tP1, vs, it > 1);
+            }
+            issue_qk<D>(tS1, q_lo0 + (kTileBytes >> 4), ks);
+            umma_commit_e(s_full(1));
+          }
+          if (it > 0) umma_commit_e(v_empty(ps));
+          umma_commit_e(k_empty(s));
         } else {
           if (it > 0) {
             if (!(ok = mbar_wait_warp(p_full(0), (it - 1) & 1))) break;
@@ -522,8 +554,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (t == 0 || has1) {
       const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
       const uint32_t tS = tmem_base + t * 128 + lane_off;
-      const uint32_t tO = tmem_base + 256 + t * kOStride + lane_off;
-      const uint32_t tP = kSplitP ? tmem_base + 384 + t * 64 + lane_off : tS;
+      const uint32_t tO = tmem_base + 256 + t * (kO1 - 256) + lane_off;
+      // This group's P columns: its own (split) or over its S columns.
+      const bool split = kSplitP || (kSplitP0 && t == 0);
+      const uint32_t tP = split ? tmem_base + kP0 + t * 64 + lane_off : tS;
       const float scale_log2 = p.scale_log2;
       float m = -INFINITY;     // reference max, base-2 scaled units
       float l = 0.0f;          // row sum of the current chunk
@@ -536,7 +570,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         uint32_t sr[128];
         float hw_max;  // max of the 128 loaded columns, from the reducing load
         tmem_ld128_max_wait(tS, sr, hw_max);
-        if constexpr (kSplitP) {
+        if (split) {
           // S_t is in registers: the next QK^T may overwrite it.
           tc_fence_before();
           mbar_arrive(s_free(t));
@@ -577,7 +611,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           m = tmax;
         }
         const float neg_m = -m;
-        if constexpr (kSplitP) {
+        if (split) {
           // P_t and O_t are free once the previous key tile's PV has completed.
           if (it > 0) {
             if (!(ok = mbar_wait_warp(o_upd(t), (it - 1) & 1))) break;
