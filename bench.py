@@ -444,10 +444,17 @@ class L2Flush:
         self.buf.zero_()
 
 
+# A spin kernel of about 1 ms queued before a timed region, so that the calls
+# after it are all enqueued before the GPU reaches the first event: the time
+# measured is the device's, not the host's launch rate.
+HOLD_CYCLES = 2_000_000
+
+
 def time_calls(fn, flush, reps, warmup=3):
     """Per-call device time of fn() (CUDA events on the current stream) with L2
     flushed before every call (outside the events); returns (median ms of the
-    flushed calls, mean ms of `reps` back-to-back calls without flushing)."""
+    flushed calls, mean ms of `reps` back-to-back calls without flushing).
+    Each timed region starts behind a spin kernel (see HOLD_CYCLES)."""
     import torch
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
@@ -455,12 +462,14 @@ def time_calls(fn, flush, reps, warmup=3):
     cold = []
     for _ in range(reps):
         flush()
+        torch.cuda._sleep(HOLD_CYCLES // 8)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         fn()
         e1.record(stream)
         e1.synchronize()
         cold.append(e0.elapsed_time(e1))
+    torch.cuda._sleep(HOLD_CYCLES)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(reps):
@@ -475,7 +484,9 @@ def measure_configs(peaks, dev, rank, reps=10):
     the CFG combine on the latent pairs the workloads name (latency: they sit
     in L2 sizes).  Inputs are drawn on the device with the workloads'
     generators.  Each launch is timed alone with L2 flushed before it
-    ("ms"); "ms_warm" is the mean of back-to-back calls with L2 warm."""
+    ("ms"); "ms_warm" is the mean of back-to-back calls with L2 warm (inputs
+    that a previous layer just wrote sit in L2 too), where consecutive
+    launches overlap their launch gap (programmatic dependent launch)."""
     import torch
     from sequence_attention_attn_b300 import dit_attn, workloads
     flush = L2Flush(dev)
