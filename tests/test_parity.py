@@ -322,3 +322,47 @@ def test_bounded_wait_times_out_without_fault():
     o_ref, l_ref = oracle.attention(f64(q), f64(k), f64(v))
     out, lse = run_attention(q, k, v, 2)                # still works afterwards
     check_attention(out, lse, o_ref, l_ref, "after timeout")
+
+
+def test_dependent_launch_chain_without_sync():
+    """Short kernels may start while the previous kernel in the stream is
+    finishing (programmatic dependent launch); each still waits for that
+    kernel's writes before reading.  A chain where every launch consumes the
+    previous one's output, with no host synchronisation in between, must
+    match the oracle applied step by step."""
+    B, H, S, D = 1, 2, 200, 64
+    q, k, v = workloads.make_random_qkv(B, H, S, D, seed=321)
+    qd, kd, vd = to_dev(q, k, v)
+    n = 3
+    parts = torch.empty((n, B * H * S, D), dtype=torch.float32, device=DEV)
+    lses = torch.empty((n, B * H * S), dtype=torch.float32, device=DEV)
+    merged = torch.empty((B * H * S, D), dtype=torch.float32, device=DEV)
+    mlse = torch.empty((B * H * S,), dtype=torch.float32, device=DEV)
+    c1 = torch.empty_like(merged)
+    c2 = torch.empty_like(merged)
+    other = torch.randn(merged.shape, generator=torch.Generator().manual_seed(5)).to(DEV)
+    q2 = torch.empty_like(qd)
+    out = torch.empty_like(qd)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=DEV)
+    torch.cuda.synchronize()
+    # partials -> merge -> two CFG combines on the merge output, all back to
+    # back; then (bf16 cast by torch) an attention whose queries are that result
+    dit_attn.dit_attn_fwd_partials(qd, kd, vd, parts, lses, n)
+    dit_attn.dit_attn_merge(parts, lses, merged, mlse)
+    dit_attn.cfg_combine(merged, other, 2.0, c1)
+    dit_attn.cfg_combine(c1, merged, 0.25, c2)
+    q2.copy_(c2.view(B, H, S, D))
+    dit_attn.dit_attn_fwd(q2, kd, vd, out, lse, 2)
+    torch.cuda.synchronize()
+    assert_no_device_error()
+    qf, kf, vf = f64(q), f64(k), f64(v)
+    m_ref, _ = oracle.lse_merge(f64(parts), f64(lses))
+    check_f32(merged, m_ref, "chain: merge of the partials")
+    c1_ref = oracle.cfg_combine(f64(merged), f64(other), 2.0)
+    check_f32(c1, c1_ref, "chain: first combine")
+    c2_ref = oracle.cfg_combine(f64(c1), f64(merged), 0.25)
+    check_f32(c2, c2_ref, "chain: second combine")
+    o_ref, l_ref = oracle.attention(f64(q2), kf, vf)
+    check_attention(out, lse, o_ref, l_ref, "chain: attention on the combined queries")
+    o1_ref, _ = oracle.attention(qf, kf, vf)
+    check_attention(merged.view(B, H, S, D), None, o1_ref, None, "chain: merged attention")
