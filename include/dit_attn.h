@@ -201,6 +201,33 @@ dit_status cfg_combine_relmae(const float *eps_c, const float *eps_u, float w,
                               float *out, long long numel, double *sums,
                               dit_stream_t stream);
 
+/* Largest numel cfg_combine_relmae_static accepts (2^28 elements). */
+#define DIT_RELMAE_STATIC_MAX_NUMEL (1LL << 28)
+
+/*
+ * cfg_combine_relmae_static -- cfg_combine_relmae with nothing asked of the
+ * caller beyond its output and nothing allocated: the per-block partial sums
+ * live in a fixed array of this library in device memory (64.25 KiB per
+ * device, found with cudaGetSymbolAddress on the first call on each device),
+ * and the last block adds them in block order, so repeated calls on the same
+ * inputs give the same bits.  The pages have no counterpart to this entry
+ * point: the fixed scratch array is this library's choice (the rel-MAE itself
+ * follows the Hybridiff page, section 2B, as for cfg_combine_relmae).
+ *
+ *   eps_c, eps_u, w, out, sums   as for cfg_combine_relmae; sums is written
+ *          (not accumulated): {sum |eps_c - eps_u|, sum |eps_u|, rel-MAE}.
+ *   numel  1 <= numel <= DIT_RELMAE_STATIC_MAX_NUMEL, else
+ *          DIT_ERR_INVALID_ARG (each block of 256 threads owns a slab of
+ *          65536 elements and the array holds 4096 slabs).
+ * The call clears the array's block counter (cudaMemsetAsync on `stream`)
+ * before its kernel.  The array is shared by every call on a device: two
+ * calls whose kernels overlap on one device (other streams, other host
+ * threads) race on it and give wrong sums; serialise them.
+ */
+dit_status cfg_combine_relmae_static(const float *eps_c, const float *eps_u,
+                                     float w, float *out, long long numel,
+                                     double *sums, dit_stream_t stream);
+
 /*
  * dit_last_device_status -- after the work queued on `stream`, reads and
  * clears this device's status word in one atomic exchange (a one-thread

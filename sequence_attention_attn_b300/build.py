@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libditattn.so")
 SOURCES = [os.path.join(CSRC, "dit_attn.cu")]
-DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("ptx.cuh", "attn_fwd.cuh", "merge_cfg.cuh")] + [
+DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("ptx.cuh", "attn_fwd.cuh", "merge_cfg.cuh", "cfg_static.cuh")] + [
     os.path.join(INCLUDE, "dit_attn.h")]
 
 NVCC_FLAGS = [

@@ -18,6 +18,7 @@
 
 #include "dit_attn.h"
 #include "attn_fwd.cuh"
+#include "cfg_static.cuh"
 #include "merge_cfg.cuh"
 #include "ptx.cuh"
 
@@ -46,6 +47,9 @@ struct DeviceState {
 };
 
 std::mutex g_mu;
+// Device address of the rel-MAE scratch array (cfg_static.cuh), looked up on
+// the first cfg_combine_relmae_static call on each device, with it current.
+double *g_relmae_scratch_ptr[kMaxDevices] = {};
 // Serialises dit_attn_fwd_torus calls: they share one event pool per device.
 std::mutex g_torus_mu;
 // Serialises status reads: they share the device word the exchange writes to.
@@ -512,6 +516,44 @@ dit_status cfg_combine_relmae(const float *eps_c, const float *eps_u, float w, f
   if (launch_pdl(ditk::cfg_combine_relmae_kernel, dim3(grid), dim3(ditk::kStreamThreads), 0, cs, eps_c, eps_u, w, out,
                  numel, sums) != cudaSuccess)
     return DIT_ERR_LAUNCH;
+  return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ERR_LAUNCH;
+}
+
+dit_status cfg_combine_relmae_static(const float *eps_c, const float *eps_u, float w, float *out, long long numel,
+                                     double *sums, dit_stream_t stream) {
+  static_assert(DIT_RELMAE_STATIC_MAX_NUMEL == ditk::kRelmaeMaxNumel, "header limit out of step");
+  if (eps_c == nullptr || eps_u == nullptr || out == nullptr || sums == nullptr) return DIT_ERR_INVALID_ARG;
+  if (numel < 1 || numel > ditk::kRelmaeMaxNumel) return DIT_ERR_INVALID_ARG;
+  if (!std::isfinite(w)) return DIT_ERR_INVALID_ARG;
+  if (!aligned16(eps_c) || !aligned16(eps_u) || !aligned16(out) || (reinterpret_cast<uintptr_t>(sums) & 7u) != 0)
+    return DIT_ERR_MISALIGNED;
+  const size_t bytes = static_cast<size_t>(numel) * 4;
+  if ((out != eps_c && ranges_overlap(out, bytes, eps_c, bytes)) ||
+      (out != eps_u && ranges_overlap(out, bytes, eps_u, bytes)) || ranges_overlap(sums, 24, eps_c, bytes) ||
+      ranges_overlap(sums, 24, eps_u, bytes) || ranges_overlap(sums, 24, out, bytes))
+    return DIT_ERR_INVALID_ARG;
+  int dev = 0;
+  DeviceState *st = nullptr;
+  dit_status s = select_device(stream, &dev, &st);
+  if (s != DIT_OK) return s;
+  double *scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_relmae_scratch_ptr[dev] == nullptr) {
+      void *p = nullptr;
+      if (cudaGetSymbolAddress(&p, ditk::g_relmae_scratch) != cudaSuccess || p == nullptr) return DIT_ERR_CUDA;
+      g_relmae_scratch_ptr[dev] = static_cast<double *>(p);
+    }
+    scratch = g_relmae_scratch_ptr[dev];
+  }
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  // The ticket counter must start at zero; the per-block slots are written
+  // before they are read.
+  if (cudaMemsetAsync(scratch + ditk::kRelmaeTicket, 0, sizeof(unsigned long long), cs) != cudaSuccess)
+    return DIT_ERR_CUDA;
+  const int grid = static_cast<int>((numel + ditk::kRelmaeSlab - 1) / ditk::kRelmaeSlab);
+  ditk::cfg_combine_relmae_slab_kernel<<<grid, ditk::kStreamThreads, 0, cs>>>(eps_c, eps_u, w, out, numel, sums,
+                                                                             scratch);
   return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ERR_LAUNCH;
 }
 

@@ -39,6 +39,7 @@ SIGNATURES = {
                             ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _vp], ctypes.c_int),
     "cfg_combine": ([_vp, _vp, ctypes.c_float, _vp, ctypes.c_longlong, _vp], ctypes.c_int),
     "cfg_combine_relmae": ([_vp, _vp, ctypes.c_float, _vp, ctypes.c_longlong, _vp, _vp], ctypes.c_int),
+    "cfg_combine_relmae_static": ([_vp, _vp, ctypes.c_float, _vp, ctypes.c_longlong, _vp, _vp], ctypes.c_int),
     "dit_last_device_status": ([_vp], ctypes.c_int),
     "dit_selftest_bounded_wait": ([_vp], ctypes.c_int),
     "dit_status_string": ([ctypes.c_int], ctypes.c_char_p),
@@ -225,6 +226,27 @@ def cfg_combine_relmae(eps_c, eps_u, w: float, out, sums, stream=None) -> None:
     rc = lib().cfg_combine_relmae(eps_c.data_ptr(), eps_u.data_ptr(), float(w), out.data_ptr(), eps_c.numel(),
                                   sums.data_ptr(), _stream(stream))
     _check(rc, "cfg_combine_relmae")
+
+
+# Largest numel cfg_combine_relmae_static accepts (DIT_RELMAE_STATIC_MAX_NUMEL).
+RELMAE_STATIC_MAX_NUMEL = 1 << 28
+
+
+def cfg_combine_relmae_static(eps_c, eps_u, w: float, out, sums, stream=None) -> None:
+    """cfg_combine_relmae with the per-block sums in the library's fixed
+    device array (no workspace, nothing allocated) and a fixed summation
+    order; numel <= RELMAE_STATIC_MAX_NUMEL.  Calls on one device must not
+    overlap (they share that array)."""
+    _need(eps_c, "eps_c", torch.float32)
+    _need(eps_u, "eps_u", torch.float32, eps_c.shape)
+    _need(out, "out", torch.float32, eps_c.shape)
+    _need(sums, "sums", torch.float64, (3,))
+    rc = lib().cfg_combine_relmae_static(eps_c.data_ptr(), eps_u.data_ptr(), float(w), out.data_ptr(),
+                                         eps_c.numel(), sums.data_ptr(), _stream(stream))
+    if rc == -1 and eps_c.numel() > RELMAE_STATIC_MAX_NUMEL:
+        raise DitError(rc, f"cfg_combine_relmae_static: numel {eps_c.numel()} is above the maximum "
+                           f"{RELMAE_STATIC_MAX_NUMEL}")
+    _check(rc, "cfg_combine_relmae_static")
 
 
 def dit_last_device_status(stream=None) -> int:
