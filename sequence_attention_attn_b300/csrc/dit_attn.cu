@@ -119,6 +119,19 @@ dit_status encode_qkv_map(CUtensorMap *map, const void *ptr, long long BH, int S
   return r == CUDA_SUCCESS ? DIT_OK : DIT_ERR_CUDA;
 }
 
+// bf16 [BH][S][D] output as a TMA store target: a box of all D columns by 32
+// rows, no swizzle (rows of D * 2 bytes, packed).
+dit_status encode_out_map(CUtensorMap *map, void *ptr, long long BH, int S, int D) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(S) * D * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(D), 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DIT_OK : DIT_ERR_CUDA;
+}
+
 // Launches a kernel with programmatic stream serialization: it may start
 // while the previous kernel in the stream finishes, and waits for it (in the
 // kernel, griddep_wait) before touching memory.
@@ -189,12 +202,16 @@ dit_status launch_attn(DeviceState &st, int didx, const void *q, const void *k, 
     mk_t = mk;
   }
   mv_t = mv;
+  // The output as a TMA store target (merged mode at D = 72; the other
+  // instantiations never read this parameter).
+  CUtensorMap mo = mq;
+  if (!kPartials && D == 72 && (s = encode_out_map(&mo, prm.out, BH, S, D)) != DIT_OK) return s;
   if (pdl) {
     if (launch_pdl(kernel, dim3(grid), dim3(ditk::kAttnThreads), L::kSmemLaunch, stream, mq, mq_t, mk, mk_t, mv,
-                   mv_t, prm) != cudaSuccess)
+                   mv_t, mo, prm) != cudaSuccess)
       return DIT_ERR_LAUNCH;
   } else {
-    kernel<<<grid, ditk::kAttnThreads, L::kSmemLaunch, stream>>>(mq, mq_t, mk, mk_t, mv, mv_t, prm);
+    kernel<<<grid, ditk::kAttnThreads, L::kSmemLaunch, stream>>>(mq, mq_t, mk, mk_t, mv, mv_t, mo, prm);
   }
   return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ERR_LAUNCH;
 }
