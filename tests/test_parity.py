@@ -324,6 +324,28 @@ def test_bounded_wait_times_out_without_fault():
     check_attention(out, lse, o_ref, l_ref, "after timeout")
 
 
+def test_attention_chain_on_its_own_output_d72():
+    """At D = 72 the merged output leaves the kernel through TMA stores.  Two
+    launches back to back, the second reading the first one's output as its
+    queries (programmatic dependent launch: it may start before the first has
+    finished and waits for its writes), then a third on the second's."""
+    B, H, S, D = 2, 3, 300, 72
+    q, k, v = workloads.make_random_qkv(B, H, S, D, seed=4242)
+    qd, kd, vd = to_dev(q, k, v)
+    o1, o2, o3 = (torch.empty_like(qd) for _ in range(3))
+    l1, l2, l3 = (torch.empty((B, H, S), dtype=torch.float32, device=DEV) for _ in range(3))
+    torch.cuda.synchronize()
+    dit_attn.dit_attn_fwd(qd, kd, vd, o1, l1, 1)
+    dit_attn.dit_attn_fwd(o1, kd, vd, o2, l2, 3)
+    dit_attn.dit_attn_fwd(o2, kd, vd, o3, l3, 1)
+    torch.cuda.synchronize()
+    assert_no_device_error()
+    kf, vf = f64(k), f64(v)
+    for qin, o, l, what in ((q, o1, l1, "first"), (o1, o2, l2, "second"), (o2, o3, l3, "third")):
+        o_ref, l_ref = oracle.attention(f64(qin), kf, vf)
+        check_attention(o, l, o_ref, l_ref, f"D=72 chain: {what} launch")
+
+
 def test_dependent_launch_chain_without_sync():
     """Short kernels may start while the previous kernel in the stream is
     finishing (programmatic dependent launch); each still waits for that
