@@ -479,6 +479,42 @@ def time_calls(fn, flush, reps, warmup=3):
     return statistics.median(cold), e0.elapsed_time(e1) / reps
 
 
+# One device's share of the heads under an 8-way head-parallel split (the
+# heads a device computes after an all-to-all), per workload.
+HEAD_SHARE = {"dit_xl2_512": 2, "pixart_1024": 2, "flux_mmdit": 3, "video": 6}
+SPLIT_COUNTS = (2, 4)
+
+
+def measure_head_share(cfg, q, k, v, heads, peaks, flush, reps):
+    """The merged launch against the chunk-parallel one (dit_attn_fwd_split at
+    SPLIT_COUNTS chunks) on the first `heads` heads of the workload: the few
+    (batch, head, query-tile pair) units of such a launch leave SMs idle,
+    which the chunks fill."""
+    import torch
+    from sequence_attention_attn_b300 import dit_attn
+    qs, ks, vs = (t[:, :heads].contiguous() for t in (q, k, v))
+    B, H, S, D = qs.shape
+    flops = 4.0 * B * H * S * S * D
+    out = torch.empty_like(qs)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=qs.device)
+
+    def rec(ms, ms_warm):
+        tf = flops / (ms / 1e3) / 1e12
+        return {"ms": ms, "tflops": tf, "frac_of_measured_burst": tf / peaks["bf16_tflops"],
+                "ms_warm": ms_warm, "tflops_warm": flops / (ms_warm / 1e3) / 1e12}
+
+    res = {"heads": heads, "B": B, "S": S, "D": D, "gflop": flops / 1e9,
+           "merged": rec(*time_calls(lambda: dit_attn.dit_attn_fwd(qs, ks, vs, out, lse, 1), flush, reps)),
+           "split": {}}
+    for n in SPLIT_COUNTS:
+        ws = torch.empty(dit_attn.dit_attn_split_workspace_bytes(B, H, S, D, n), dtype=torch.uint8,
+                         device=qs.device)
+        res["split"][str(n)] = rec(*time_calls(lambda: dit_attn.dit_attn_fwd_split(qs, ks, vs, out, lse, n, ws),
+                                               flush, reps))
+        del ws
+    return res
+
+
 def measure_configs(peaks, dev, rank, reps=10):
     """Attention TFLOP/s of every workload at each chunk count it lists, plus
     the CFG combine on the latent pairs the workloads name (latency: they sit
@@ -503,6 +539,9 @@ def measure_configs(peaks, dev, rank, reps=10):
                 "ms": ms, "tflops": tf, "frac_of_measured_burst": tf / peaks["bf16_tflops"],
                 "frac_of_nominal_2250": tf / NOMINAL_BF16_TFLOPS,
                 "ms_warm": ms_warm, "tflops_warm": cfg.flops / (ms_warm / 1e3) / 1e12}
+        share = HEAD_SHARE.get(cfg.name)
+        if share is not None:
+            entry["head_share"] = measure_head_share(cfg, q, k, v, share, peaks, flush, reps)
         if cfg.cfg_shape is not None:
             eps_c, eps_u = workloads.make_cfg(cfg.cfg_shape, seed=workloads.seed_for(cfg, 100), device=dev)
             c_out = torch.empty_like(eps_c)

@@ -94,6 +94,47 @@ dit_status dit_attn_fwd_partials(const void *q, const void *k, const void *v,
                                  dit_stream_t stream);
 
 /*
+ * dit_attn_fwd_split -- dit_attn_fwd computed chunk-parallel: one CTA per
+ * (query-tile pair, chunk c of the balanced partition into n_split chunks)
+ * writes the chunk's normalised fp32 partial O_c and LSE_c to the caller's
+ * workspace (dit_attn_fwd_partials), then a second kernel merges the chunks
+ * of every row by their log-sum-exp weights and writes out (bf16) and lse.
+ * It serves launches with few (batch, head, query-tile pair) units, such as
+ * one device's share of the heads under a head-parallel split, where the
+ * merged launch leaves SMs idle: each chunk adds a CTA per pair.  Source:
+ * "xDiT: an Inference Engine for DiTs with Massive Parallelism" (abstract:
+ * sequence parallelism splits the attention of a long token sequence);
+ * "SwiftFusion ..." (ideas 1 and 2: every piece of K/V yields a partial
+ * result, folded in by its log-sum-exp).  Same result as dit_attn_fwd with
+ * n_kv_chunks = n_split, up to rounding.
+ *
+ *   q, k, v, out, lse, B, H, S, D   as for dit_attn_fwd.
+ *   n_split    1 <= n_split <= S (else DIT_ERR_INVALID_ARG).
+ *   workspace  device memory of at least
+ *              dit_attn_split_workspace_bytes(B, H, S, D, n_split) bytes,
+ *              16-byte aligned, overlapping no other buffer of the call;
+ *              owned by the caller, reusable by later calls on the same
+ *              stream (nothing in it needs clearing).  Calls that share one
+ *              workspace must not overlap on the GPU.
+ *   workspace_bytes  its size (too small: DIT_ERR_INVALID_ARG).
+ * Launches the partials kernel, then the merge kernel as a programmatic
+ * dependent launch on the same stream (it may start while the first kernel's
+ * last CTAs run and waits for all of them before reading the workspace).
+ */
+dit_status dit_attn_fwd_split(const void *q, const void *k, const void *v,
+                              void *out, float *lse, int B, int H, int S, int D,
+                              int n_split, void *workspace,
+                              size_t workspace_bytes, dit_stream_t stream);
+
+/*
+ * dit_attn_split_workspace_bytes -- the workspace dit_attn_fwd_split needs:
+ * fp32 partials [n_split, B * H * S, D] followed, from the next 256-byte
+ * boundary, by their LSEs [n_split, B * H * S], padded to 256 bytes.
+ * Returns 0 for invalid sizes or an unsupported D.
+ */
+size_t dit_attn_split_workspace_bytes(int B, int H, int S, int D, int n_split);
+
+/*
  * dit_attn_fwd_range -- attention of every query over one key range
  * [j0, j1): the computation a device of a ring / Torus sequence-parallel
  * split performs on the piece of K/V it holds ("SwiftFusion ...", ideas 1 and

@@ -278,6 +278,19 @@ dit_status attn_dispatch(const void *q, const void *k, const void *v, void *out,
   }
 }
 
+// Workspace of dit_attn_fwd_split: fp32 partials [n][rows][D], then their
+// LSEs [n][rows] from the next 256-byte boundary.
+struct SplitWorkspace {
+  size_t lse_off, total;
+};
+SplitWorkspace split_workspace(long long rows, int D, int n) {
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  SplitWorkspace w;
+  w.lse_off = up(static_cast<size_t>(n) * rows * D * 4);
+  w.total = w.lse_off + up(static_cast<size_t>(n) * rows * 4);
+  return w;
+}
+
 int stream_grid(const DeviceState &st, long long work_items) {
   const long long per_wave = static_cast<long long>(st.sm_count) * 8;
   const long long need = (work_items + ditk::kStreamThreads - 1) / ditk::kStreamThreads;
@@ -348,6 +361,54 @@ dit_status dit_attn_fwd_partials(const void *q, const void *k, const void *v, fl
       ranges_overlap(lses, l_bytes, partials, p_bytes))
     return DIT_ERR_INVALID_ARG;
   return attn_dispatch<true>(q, k, v, nullptr, nullptr, partials, lses, B, H, S, D, n_kv_chunks, stream);
+}
+
+size_t dit_attn_split_workspace_bytes(int B, int H, int S, int D, int n_split) {
+  if (B < 1 || H < 1 || S < 1 || n_split < 1 || n_split > S || head_dim_index(D) < 0) return 0;
+  if (static_cast<long long>(B) * H > 2147483647LL) return 0;
+  return split_workspace(static_cast<long long>(B) * H * S, D, n_split).total;
+}
+
+dit_status dit_attn_fwd_split(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
+                              int S, int D, int n_split, void *workspace, size_t workspace_bytes,
+                              dit_stream_t stream) {
+  dit_status s = check_attn_args(q, k, v, B, H, S, D, n_split);
+  if (s != DIT_OK) return s;
+  if (out == nullptr || workspace == nullptr) return DIT_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(workspace) || (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0))
+    return DIT_ERR_MISALIGNED;
+  const long long rows = static_cast<long long>(B) * H * S;
+  const SplitWorkspace w = split_workspace(rows, D, n_split);
+  if (workspace_bytes < w.total) return DIT_ERR_INVALID_ARG;
+  const size_t bytes = static_cast<size_t>(rows) * D * 2, lb = static_cast<size_t>(rows) * 4;
+  const void *inputs[] = {q, k, v};
+  for (const void *b : inputs) {
+    if (ranges_overlap(out, bytes, b, bytes) || ranges_overlap(workspace, w.total, b, bytes) ||
+        (lse != nullptr && ranges_overlap(lse, lb, b, bytes)))
+      return DIT_ERR_INVALID_ARG;
+  }
+  if (ranges_overlap(workspace, w.total, out, bytes) ||
+      (lse != nullptr && (ranges_overlap(lse, lb, out, bytes) || ranges_overlap(lse, lb, workspace, w.total))))
+    return DIT_ERR_INVALID_ARG;
+  float *partials = static_cast<float *>(workspace);
+  float *lses = reinterpret_cast<float *>(static_cast<char *>(workspace) + w.lse_off);
+  // One CTA per (query-tile pair, chunk): each chunk's normalised partial
+  // and LSE to the workspace ...
+  if ((s = attn_dispatch<true>(q, k, v, nullptr, nullptr, partials, lses, B, H, S, D, n_split, stream)) != DIT_OK)
+    return s;
+  // ... then their log-sum-exp merge over all rows, rounded to bf16 (a
+  // programmatic launch: it starts as the attention CTAs finish and waits
+  // for all of them before reading the workspace).
+  int dev = 0;
+  DeviceState *st = nullptr;
+  if ((s = select_device(stream, &dev, &st)) != DIT_OK) return s;
+  const int d4 = D / 4;
+  if (launch_pdl(ditk::lse_merge_bf16_kernel, dim3(stream_grid(*st, rows * d4)), dim3(ditk::kStreamThreads), 0,
+                 reinterpret_cast<cudaStream_t>(stream), static_cast<const float *>(partials),
+                 static_cast<const float *>(lses), n_split, static_cast<__nv_bfloat16 *>(out), lse, rows,
+                 d4) != cudaSuccess)
+    return DIT_ERR_LAUNCH;
+  return cudaGetLastError() == cudaSuccess ? DIT_OK : DIT_ERR_LAUNCH;
 }
 
 dit_status dit_attn_fwd_range(const void *q, const void *k, const void *v, float *out, float *lse, int B, int H,

@@ -22,6 +22,7 @@
 // (programmatic dependent launch, see ptx.cuh).
 #pragma once
 #include <cstdint>
+#include <cuda_bf16.h>
 
 #include "ptx.cuh"
 
@@ -80,6 +81,46 @@ __global__ void __launch_bounds__(kStreamThreads)
       }
     }
     st_stream(reinterpret_cast<float4 *>(out) + idx, acc);
+    if (lse_out != nullptr && c4 == 0) lse_out[r] = lse;
+  }
+}
+
+// As lse_merge_vec4_kernel, with the merged row rounded to bf16 (one 8-byte
+// store per 4 columns): the second half of the chunk-parallel attention
+// launch (dit_attn_fwd_split), writing the [B, H, S, D] bf16 output.
+__global__ void __launch_bounds__(kStreamThreads)
+    lse_merge_bf16_kernel(const float *__restrict__ partials, const float *__restrict__ lses, int n,
+                          __nv_bfloat16 *__restrict__ out, float *__restrict__ lse_out, long long rows, int d4) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const long long total = rows * d4;
+  const long long stride = static_cast<long long>(gridDim.x) * kStreamThreads;
+  for (long long idx = static_cast<long long>(blockIdx.x) * kStreamThreads + threadIdx.x; idx < total;
+       idx += stride) {
+    const long long r = idx / d4;
+    const int c4 = static_cast<int>(idx - r * d4);
+    const float lse = merged_lse(lses, n, rows, r);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lse != -INFINITY) {
+      const float4 *src = reinterpret_cast<const float4 *>(partials) + r * d4 + c4;
+      const long long cstride = rows * d4;
+#pragma unroll 8
+      for (int c = 0; c < n; ++c) {
+        const float l = __ldg(lses + c * rows + r);
+        const float4 v = ld_stream(src + c * cstride);
+        if (l != -INFINITY) {
+          const float w = __expf(l - lse);
+          acc.x = fmaf(w, v.x, acc.x);
+          acc.y = fmaf(w, v.y, acc.y);
+          acc.z = fmaf(w, v.z, acc.z);
+          acc.w = fmaf(w, v.w, acc.w);
+        }
+      }
+    }
+    uint2 o;
+    o.x = pack_bf16x2(acc.x, acc.y);
+    o.y = pack_bf16x2(acc.z, acc.w);
+    reinterpret_cast<uint2 *>(out)[idx] = o;
     if (lse_out != nullptr && c4 == 0) lse_out[r] = lse;
   }
 }

@@ -37,6 +37,9 @@ SIGNATURES = {
                             ctypes.c_int, ctypes.c_int, _vp], ctypes.c_int),
     "dit_attn_fwd_torus": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, ctypes.c_int,
                             ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _vp], ctypes.c_int),
+    "dit_attn_fwd_split": ([_vp, _vp, _vp, _vp, _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                            ctypes.c_int, _vp, ctypes.c_size_t, _vp], ctypes.c_int),
+    "dit_attn_split_workspace_bytes": ([ctypes.c_int] * 5, ctypes.c_size_t),
     "cfg_combine": ([_vp, _vp, ctypes.c_float, _vp, ctypes.c_longlong, _vp], ctypes.c_int),
     "cfg_combine_relmae": ([_vp, _vp, ctypes.c_float, _vp, ctypes.c_longlong, _vp, _vp], ctypes.c_int),
     "cfg_combine_relmae_static": ([_vp, _vp, ctypes.c_float, _vp, ctypes.c_longlong, _vp, _vp], ctypes.c_int),
@@ -139,6 +142,31 @@ def dit_attn_fwd_partials(q, k, v, partials, lses, n_kv_chunks: int, stream=None
     rc = lib().dit_attn_fwd_partials(q.data_ptr(), k.data_ptr(), v.data_ptr(), partials.data_ptr(),
                                      lses.data_ptr(), B, H, S, D, n, _stream(stream))
     _check(rc, "dit_attn_fwd_partials")
+
+
+def dit_attn_split_workspace_bytes(B: int, H: int, S: int, D: int, n_split: int) -> int:
+    """Bytes of workspace dit_attn_fwd_split needs (0 for invalid sizes)."""
+    return int(lib().dit_attn_split_workspace_bytes(int(B), int(H), int(S), int(D), int(n_split)))
+
+
+def dit_attn_fwd_split(q, k, v, out, lse, n_split: int, workspace, stream=None) -> None:
+    """Chunk-parallel attention: q, k, v, out bf16 [B, H, S, D]; lse fp32
+    [B, H, S] or None; workspace a uint8 CUDA tensor of at least
+    dit_attn_split_workspace_bytes(...) bytes."""
+    _need(q, "q", torch.bfloat16)
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, S, D]")
+    B, H, S, D = q.shape
+    _need(k, "k", torch.bfloat16, q.shape)
+    _need(v, "v", torch.bfloat16, q.shape)
+    _need(out, "out", torch.bfloat16, q.shape)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (B, H, S))
+    _need(workspace, "workspace", torch.uint8)
+    rc = lib().dit_attn_fwd_split(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                  None if lse is None else lse.data_ptr(), B, H, S, D, int(n_split),
+                                  workspace.data_ptr(), workspace.numel(), _stream(stream))
+    _check(rc, "dit_attn_fwd_split")
 
 
 def dit_attn_merge(partials, lses, out, lse_out=None, stream=None) -> None:
@@ -264,6 +292,19 @@ def attention(q, k, v, n_kv_chunks: int = 1, with_lse: bool = True, stream=None)
     out = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device) if with_lse else None
     dit_attn_fwd(q, k, v, out, lse, n_kv_chunks, stream)
+    return out, lse
+
+
+def attention_split(q, k, v, n_split: int, with_lse: bool = True, stream=None):
+    """dit_attn_fwd_split with the outputs and the workspace allocated by torch; returns (out, lse)."""
+    B, H, S, D = q.shape
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device) if with_lse else None
+    nbytes = dit_attn_split_workspace_bytes(B, H, S, D, n_split)
+    if nbytes == 0:
+        raise ValueError("invalid sizes for the split launch")
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    dit_attn_fwd_split(q, k, v, out, lse, n_split, ws, stream)
     return out, lse
 
 

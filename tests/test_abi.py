@@ -170,3 +170,30 @@ def test_torus_rejects_bad_arguments_on_host(lib):
     assert call(ks=V) == INVALID                  # k_src is v: chunk copies into v overwrite it
     assert call(vs=K + 64) == INVALID             # v_src overlaps k
     assert call(ls=P + 64) == INVALID             # lses inside partials
+
+
+def test_split_workspace_size_and_host_checks(lib):
+    sz = lib.dit_attn_split_workspace_bytes
+    rows, D, n = 2 * 16 * 1024, 72, 4
+    up = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    assert sz(2, 16, 1024, 72, 4) == up(n * rows * D * 4) + up(n * rows * 4)
+    assert sz(2, 16, 1024, 65, 4) == 0 and sz(0, 16, 1024, 72, 4) == 0
+    assert sz(2, 16, 1024, 72, 0) == 0 and sz(1, 1, 8, 64, 9) == 0   # n_split past S
+    f = lib.dit_attn_fwd_split
+    W = 0x7F5000000000
+    nb = sz(1, 2, 256, 64, 2)
+
+    def call(q=A, out=O, lse=L, ws=W, wsb=nb, S=256, D=64, ns=2):
+        return f(q, B_, C, out, lse, 1, 2, S, D, ns, ws, wsb, None)
+
+    assert call(ws=None) == INVALID
+    assert call(out=None) == INVALID
+    assert call(ns=0) == INVALID
+    assert call(ns=257) == INVALID              # more chunks than keys
+    assert call(wsb=nb - 1) == INVALID          # workspace too small
+    assert call(ws=W + 8) == MISALIGNED
+    assert call(lse=L + 2) == MISALIGNED
+    assert call(ws=A + 64) == INVALID           # workspace over q
+    assert call(ws=O) == INVALID                # workspace over out
+    assert call(lse=W + 64) == INVALID          # lse inside the workspace
+    assert call(D=96) == SHAPE
