@@ -109,7 +109,9 @@ dit_status dit_attn_fwd_partials(const void *q, const void *k, const void *v,
  * n_kv_chunks = n_split, up to rounding.
  *
  *   q, k, v, out, lse, B, H, S, D   as for dit_attn_fwd.
- *   n_split    1 <= n_split <= S (else DIT_ERR_INVALID_ARG).
+ *   n_split    1 <= n_split <= S (else DIT_ERR_INVALID_ARG); the partials
+ *              must fit the merge's limits (B * H * S * D < 2^40 and
+ *              n_split * B * H * S * D <= 2^46).
  *   workspace  device memory of at least
  *              dit_attn_split_workspace_bytes(B, H, S, D, n_split) bytes,
  *              16-byte aligned, overlapping no other buffer of the call;
@@ -130,7 +132,8 @@ dit_status dit_attn_fwd_split(const void *q, const void *k, const void *v,
  * dit_attn_split_workspace_bytes -- the workspace dit_attn_fwd_split needs:
  * fp32 partials [n_split, B * H * S, D] followed, from the next 256-byte
  * boundary, by their LSEs [n_split, B * H * S], padded to 256 bytes.
- * Returns 0 for invalid sizes or an unsupported D.
+ * Returns 0 for invalid sizes (those dit_attn_fwd_split rejects) or an
+ * unsupported D.
  */
 size_t dit_attn_split_workspace_bytes(int B, int H, int S, int D, int n_split);
 

@@ -363,10 +363,17 @@ dit_status dit_attn_fwd_partials(const void *q, const void *k, const void *v, fl
   return attn_dispatch<true>(q, k, v, nullptr, nullptr, partials, lses, B, H, S, D, n_kv_chunks, stream);
 }
 
+// The merge kernel's size limits: rows * D < 2^40, n * rows * D <= 2^46.
+bool split_sizes_ok(long long rows, int D, int n) {
+  return rows <= (1LL << 40) / D && static_cast<long long>(n) * rows * D <= (1LL << 46);
+}
+
 size_t dit_attn_split_workspace_bytes(int B, int H, int S, int D, int n_split) {
   if (B < 1 || H < 1 || S < 1 || n_split < 1 || n_split > S || head_dim_index(D) < 0) return 0;
   if (static_cast<long long>(B) * H > 2147483647LL) return 0;
-  return split_workspace(static_cast<long long>(B) * H * S, D, n_split).total;
+  const long long rows = static_cast<long long>(B) * H * S;
+  if (!split_sizes_ok(rows, D, n_split)) return 0;
+  return split_workspace(rows, D, n_split).total;
 }
 
 dit_status dit_attn_fwd_split(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
@@ -378,6 +385,7 @@ dit_status dit_attn_fwd_split(const void *q, const void *k, const void *v, void 
   if (!aligned16(out) || !aligned16(workspace) || (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0))
     return DIT_ERR_MISALIGNED;
   const long long rows = static_cast<long long>(B) * H * S;
+  if (!split_sizes_ok(rows, D, n_split)) return DIT_ERR_INVALID_ARG;
   const SplitWorkspace w = split_workspace(rows, D, n_split);
   if (workspace_bytes < w.total) return DIT_ERR_INVALID_ARG;
   const size_t bytes = static_cast<size_t>(rows) * D * 2, lb = static_cast<size_t>(rows) * 4;

@@ -197,3 +197,10 @@ def test_split_workspace_size_and_host_checks(lib):
     assert call(ws=O) == INVALID                # workspace over out
     assert call(lse=W + 64) == INVALID          # lse inside the workspace
     assert call(D=96) == SHAPE
+
+
+def test_split_rejects_partials_past_the_merge_limits(lib):
+    # 2^47 partial elements: refused by the size query and the call alike
+    assert lib.dit_attn_split_workspace_bytes(1, 1 << 14, 1 << 16, 128, 1 << 10) == 0
+    assert lib.dit_attn_fwd_split(A, B_, C, O, L, 1, 1 << 14, 1 << 16, 128, 1 << 10,
+                                  0x7F5000000000, 1 << 62, None) == INVALID
