@@ -189,16 +189,20 @@ constexpr uint32_t kHi32 = desc_hi(256, kSwizzle32B);
 template <int D>
 __device__ __forceinline__ void issue_qk(uint32_t tS, uint32_t q_lo, uint32_t k_lo) {
   constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, kBlockN, false);
-#pragma unroll
-  for (int ks = 0; ks < 4; ++ks)
-    umma_ss_e(tS, q_lo + 2 * ks, kHi128, k_lo + 2 * ks, kHi128, idesc, ks > 0 ? 1u : 0u);
   constexpr uint32_t kBlk = kSwzBytes >> 4;
   if constexpr (D == 128) {
+    // Both 64-column blocks of the head dimension, four K = 16 steps each, in
+    // two issue blocks (one elected lane, descriptors stepped in registers):
+    // fewer instructions on the issuing warp's sub-partition, which it shares
+    // with two softmax warps (+3 % on Flux; at D = 64 and 72 the per-MMA form
+    // measured as fast or faster and stays).
+    umma_ss4_e(tS, desc64(q_lo, kHi128), desc64(k_lo, kHi128), idesc, 0u);
+    umma_ss4_e(tS, desc64(q_lo + kBlk, kHi128), desc64(k_lo + kBlk, kHi128), idesc, 1u);
+  } else {
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
-      umma_ss_e(tS, q_lo + kBlk + 2 * ks, kHi128, k_lo + kBlk + 2 * ks, kHi128, idesc, 1u);
-  } else if constexpr (D == 72) {
-    umma_ss_e(tS, q_lo + kBlk, kHi32, k_lo + kBlk, kHi32, idesc, 1u);
+      umma_ss_e(tS, q_lo + 2 * ks, kHi128, k_lo + 2 * ks, kHi128, idesc, ks > 0 ? 1u : 0u);
+    if constexpr (D == 72) umma_ss_e(tS, q_lo + kBlk, kHi32, k_lo + kBlk, kHi32, idesc, 1u);
   }
 }
 
@@ -209,10 +213,14 @@ __device__ __forceinline__ void issue_qk(uint32_t tS, uint32_t q_lo, uint32_t k_
 template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_lo, bool accumulate) {
   constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, AttnCfg<D>::kDpad, true);
+  if constexpr (D == 128) {
+    umma_ts8_e(tO, tP, desc64(v_lo, kHi128), idesc, accumulate ? 1u : 0u);
+  } else {
 #pragma unroll
-  for (int ks = 0; ks < kBlockN / 16; ++ks) {
-    const uint32_t acc = (accumulate || ks > 0) ? 1u : 0u;
-    umma_ts_e(tO, tP + ks * 8, v_lo + ks * (2048 >> 4), kHi128, idesc, acc);
+    for (int ks = 0; ks < kBlockN / 16; ++ks) {
+      const uint32_t acc = (accumulate || ks > 0) ? 1u : 0u;
+      umma_ts_e(tO, tP + ks * 8, v_lo + ks * (2048 >> 4), kHi128, idesc, acc);
+    }
   }
 }
 

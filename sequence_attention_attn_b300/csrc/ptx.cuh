@@ -230,6 +230,51 @@ __device__ __forceinline__ void umma_ts_e(uint32_t d_tmem, uint32_t a_tmem, uint
       "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Four K = 16 steps of D[tmem] (+)= A[smem] * B[smem]^T in one block, one
+// elected lane (the same one as every other call of a converged warp): both
+// descriptors advance by 32 bytes a step (2 in the start-address field); the
+// first step accumulates only if acc0 != 0, the others always.
+__device__ __forceinline__ void umma_ss4_e(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred e, p0, p1;\n\t.reg .b64 da, db;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p0, %4, 0;\n\t"
+      "setp.eq.b32 p1, %3, %3;\n\t"
+      "mov.b64 da, %1;\n\tmov.b64 db, %2;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p0;\n\t"
+      "add.s64 da, da, 2;\n\tadd.s64 db, db, 2;\n\t" "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p1;\n\t"
+      "add.s64 da, da, 2;\n\tadd.s64 db, db, 2;\n\t" "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p1;\n\t"
+      "add.s64 da, da, 2;\n\tadd.s64 db, db, 2;\n\t" "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p1;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc0)
+      : "memory");
+}
+// Eight K = 16 steps of D[tmem] (+)= A[tmem] * B[smem] in one block: A
+// advances 8 TMEM columns a step, B's descriptor 2048 bytes (128 in the
+// start-address field); the first step accumulates only if acc0 != 0.
+__device__ __forceinline__ void umma_ts8_e(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred e, p0, p1;\n\t.reg .b64 db;\n\t.reg .b32 ta;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p0, %4, 0;\n\t"
+      "setp.eq.b32 p1, %3, %3;\n\t"
+      "mov.b32 ta, %1;\n\tmov.b64 db, %2;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, p0;\n\t"
+      "add.u32 ta, ta, 8;\n\tadd.s64 db, db, 128;\n\t" "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, p1;\n\t"
+      "add.u32 ta, ta, 8;\n\tadd.s64 db, db, 128;\n\t" "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, p1;\n\t"
+      "add.u32 ta, ta, 8;\n\tadd.s64 db, db, 128;\n\t" "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, p1;\n\t"
+      "add.u32 ta, ta, 8;\n\tadd.s64 db, db, 128;\n\t" "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, p1;\n\t"
+      "add.u32 ta, ta, 8;\n\tadd.s64 db, db, 128;\n\t" "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, p1;\n\t"
+      "add.u32 ta, ta, 8;\n\tadd.s64 db, db, 128;\n\t" "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, p1;\n\t"
+      "add.u32 ta, ta, 8;\n\tadd.s64 db, db, 128;\n\t" "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, p1;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc0)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t desc64(uint32_t lo, uint32_t hi) {
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
 __device__ __forceinline__ void umma_commit_e(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
