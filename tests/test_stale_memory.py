@@ -1,7 +1,8 @@
-"""GPU parity of the attention launches when the memory under their buffers
-held NaN just before: blocks filled with NaN are freed, the inputs are copied
-from pageable host memory into them (the copy is the last operation before the
-launch), and the output, LSE and partial buffers are left uninitialised.  A
+"""GPU parity of the attention launches (merged, partials + merge,
+chunk-parallel) when the memory under their buffers held NaN just before:
+blocks filled with NaN are freed, the inputs are copied from pageable host
+memory into them (the copy is the last operation before the launch), and the
+output, LSE, partial and workspace buffers are left uninitialised.  A
 launch that read past its inputs, read an output buffer or left part of it
 unwritten would show non-finite values here.  Repeated three times in one
 process, so the later calls run on memory the earlier ones released."""
@@ -50,3 +51,8 @@ def test_merged_and_partials_over_stale_nan_memory(D):
                 assert np.isfinite(m).all(), f"rep={rep} S={S} D={D} n={n}: non-finite merge"
                 check_attention(merged.to(torch.bfloat16), mlse, o_ref, l_ref,
                                 f"rep={rep} S={S} D={D} n={n} partials+merge", abs_ref=a_ref)
+                qd, kd, vd = upload_over_nan(q, k, v)
+                sout, slse = dit_attn.attention_split(qd, kd, vd, n)
+                torch.cuda.synchronize()
+                assert dit_attn.dit_last_device_status() == 0
+                check_attention(sout, slse, o_ref, l_ref, f"rep={rep} S={S} D={D} n={n} split", abs_ref=a_ref)
