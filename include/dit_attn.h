@@ -1,13 +1,17 @@
 /*
  * dit_attn.h -- C ABI of libditattn.so: blockwise DiT attention with on-chip
- * chunk merging, the standalone log-sum-exp merge and the classifier-free
- * guidance combine, for NVIDIA B300 (sm_103a).
+ * chunk merging (and its per-chunk, key-range, Torus-pipelined and
+ * chunk-parallel forms), the standalone log-sum-exp merge, and the
+ * classifier-free guidance combine with its fused rel-MAE, for NVIDIA B300
+ * (sm_103a).
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- *  - Every pointer is a DEVICE pointer owned by the caller.  The library
- *    allocates no memory on any call path; it keeps one 4-byte device status
- *    word per device in a static __device__ variable.
+ *  - Every pointer is a DEVICE pointer owned by the caller (dit_attn_fwd_torus
+ *    also takes pinned host sources).  The library allocates no memory on any
+ *    call path; per device it keeps, in static __device__ variables, a 4-byte
+ *    status word with its read-back copy and the 64.25 KiB scratch array of
+ *    cfg_combine_relmae_static.
  *  - Calls are asynchronous on `stream` (NULL = the legacy default stream of
  *    the current device) and return after the launch.  A status other than
  *    DIT_OK means nothing was launched, except DIT_ERR_LAUNCH.
