@@ -560,7 +560,8 @@ def measure_configs(peaks, dev, rank, reps=10):
 
 
 def cfg_hbm_sweep(peaks, dev, sizes=(1 << 24, 1 << 26, 1 << 28), reps=10):
-    """The CFG combine and its rel-MAE-fused form on operands larger than L2
+    """The CFG combine and its rel-MAE-fused forms (device atomics, and the
+    no-workspace form with a fixed summation order) on operands larger than L2
     (2^24, 2^26 and 2^28 fp32 elements each: 0.2, 0.8 and 3.2 GB of
     algorithmic traffic per call), outside the timed step: the bandwidth
     figure the workload latents (L2-resident) cannot show.  The top-level
@@ -578,7 +579,9 @@ def cfg_hbm_sweep(peaks, dev, sizes=(1 << 24, 1 << 26, 1 << 28), reps=10):
         res = {"numel_per_operand": numel, "bytes_per_call": 12.0 * numel, "l2": "operands larger than L2; no flush"}
         for name, fn in (("cfg_combine", lambda: dit_attn.cfg_combine(c, u, 4.5, o, stream.cuda_stream)),
                          ("cfg_combine_relmae", lambda: dit_attn.cfg_combine_relmae(c, u, 4.5, o, sums,
-                                                                                    stream.cuda_stream))):
+                                                                                    stream.cuda_stream)),
+                         ("cfg_combine_relmae_static",
+                          lambda: dit_attn.cfg_combine_relmae_static(c, u, 4.5, o, sums, stream.cuda_stream))):
             for _ in range(3):
                 fn()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -598,7 +601,9 @@ def cfg_hbm_sweep(peaks, dev, sizes=(1 << 24, 1 << 26, 1 << 28), reps=10):
     main = next(r for r in sweep if r["numel_per_operand"] == 1 << 26) if (1 << 26) in sizes else sweep[-1]
     return {**main, "sweep": [{"numel_per_operand": r["numel_per_operand"],
                                "cfg_combine_gbs": r["cfg_combine"]["gbs"],
-                               "cfg_combine_relmae_gbs": r["cfg_combine_relmae"]["gbs"]} for r in sweep]}
+                               "cfg_combine_relmae_gbs": r["cfg_combine_relmae"]["gbs"],
+                               "cfg_combine_relmae_static_gbs": r["cfg_combine_relmae_static"]["gbs"]}
+                              for r in sweep]}
 
 
 def torus_overlap(q, k, v, cfg, dev, n, reps=5):
