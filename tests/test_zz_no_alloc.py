@@ -10,11 +10,11 @@ import oracle
 from sequence_attention_attn_b300 import dit_attn, workloads
 
 DEV = "cuda:0"
-INVALID = -1
+INVALID, MISALIGNED = -1, -3
 NAN = float("nan")
 
 
-def test_static_relmae_rejects_bad_sizes_on_host():
+def test_static_relmae_rejects_bad_arguments_on_host():
     # rejected before any CUDA call: the (never dereferenced) pointers are fake
     f = dit_attn.lib().cfg_combine_relmae_static
     A, B, O, S = 0x7F0000000000, 0x7F1000000000, 0x7F2000000000, 0x7F3000000000
@@ -22,6 +22,10 @@ def test_static_relmae_rejects_bad_sizes_on_host():
     assert f(A, B, 1.5, O, 0, S, None) == INVALID
     assert f(None, B, 1.5, O, 16, S, None) == INVALID
     assert f(A, B, float("inf"), O, 16, S, None) == INVALID
+    assert f(A + 8, B, 1.5, O, 16, S, None) == MISALIGNED      # eps_c not 16-byte aligned
+    assert f(A, B, 1.5, O, 16, S + 4, None) == MISALIGNED      # sums not 8-byte aligned
+    assert f(A, B, 1.5, A + 16, 16, S, None) == INVALID        # out overlaps eps_c, not equal to it
+    assert f(A, B, 1.5, O, 16, B + 8, None) == INVALID         # sums inside eps_u
 
 
 def run_both(c, u, w):
