@@ -731,8 +731,20 @@ def run_e2e(args, q, k, v, parts, part_lse, eps_c, eps_u, out, lse, m_out, m_lse
     torch.cuda.synchronize()
     dt = time.perf_counter() - t0
     max_s, units = reduce_time_and_units(dt, cfg.flops * args.e2e_steps, world, dev)
+    # The host link alone, after the timed steps: the largest input (the merge
+    # partials) copied once from pinned memory, CUDA events on the copy's
+    # stream.  The step cannot be faster than its H2D bytes at this rate.
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    parts.copy_(h_in[3], non_blocking=True)
+    e1.record(stream)
+    e1.synchronize()
+    link_gbs = parts.numel() * parts.element_size() / (e0.elapsed_time(e1) / 1e3) / 1e9
+    ms_step = 1e3 * max_s / args.e2e_steps
+    bound_ms = h2d / (link_gbs * 1e9) * 1e3
     return {"value": units / max_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": args.e2e_steps, "ms_per_step": 1e3 * max_s / args.e2e_steps}
+            "d2h_bytes_per_step": d2h, "steps": args.e2e_steps, "ms_per_step": ms_step,
+            "host_h2d_gbs": link_gbs, "h2d_bound_ms": bound_ms, "frac_of_h2d_bound": bound_ms / ms_step}
 
 
 def main(argv=None):
