@@ -246,16 +246,24 @@ def test_attention_edge_lengths_unit_std(S, D):
         check_attention(out, lse, o_ref, l_ref, f"std 1 S={S} D={D} n={n}")
 
 
-def test_attention_chunks_shorter_than_a_tile():
-    # 40 chunks of 6-7 keys: every tile is cut at a chunk end
-    q, k, v = workloads.make_random_qkv(2, 2, 260, 64, seed=99, std=2.0)
+@pytest.mark.parametrize("D", [64, 72, 128])
+def test_attention_chunks_shorter_than_a_tile(D):
+    # 40 chunks of 6-7 keys: every tile is cut at a chunk end; then one key
+    # per chunk, merged on chip and as S one-key partials merged afterwards
+    S = 260
+    q, k, v = workloads.make_random_qkv(2, 2, S, D, seed=99 + D, std=2.0)
     qf, kf, vf = f64(q), f64(k), f64(v)
     o_ref, l_ref = oracle.attention(qf, kf, vf)
     a_ref = abs_weighted(qf, kf, vf)
     out, lse = run_attention(q, k, v, 40)
-    check_attention(out, lse, o_ref, l_ref, "n=40", abs_ref=a_ref)
-    out, lse = run_attention(q, k, v, 260)   # one key per chunk
-    check_attention(out, lse, o_ref, l_ref, "n=S", abs_ref=a_ref)
+    check_attention(out, lse, o_ref, l_ref, f"D={D} n=40", abs_ref=a_ref)
+    out, lse = run_attention(q, k, v, S)
+    check_attention(out, lse, o_ref, l_ref, f"D={D} n=S", abs_ref=a_ref)
+    parts, lses = dit_attn.attention_partials(*to_dev(q, k, v), S)
+    merged, mlse = dit_attn.merge(parts, lses)
+    torch.cuda.synchronize()
+    assert_no_device_error()
+    check_attention(merged.to(torch.bfloat16), mlse, o_ref, l_ref, f"D={D} n=S partials+merge", abs_ref=a_ref)
 
 
 def test_attention_sharp_softmax():
