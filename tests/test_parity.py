@@ -279,13 +279,18 @@ def test_attention_sharp_softmax(D):
         check_attention(out, lse, o_ref, l_ref, f"sharp D={D} n={n}", abs_ref=a_ref)
 
 
-def test_attention_without_lse_output():
-    q, k, v = workloads.make_random_qkv(1, 2, 300, 72, seed=8)
+@pytest.mark.parametrize("D", [64, 72, 128])
+def test_attention_without_lse_output(D):
+    q, k, v = workloads.make_random_qkv(1, 2, 300, D, seed=8)
     o_ref, _ = oracle.attention(f64(q), f64(k), f64(v))
     qd, kd, vd = to_dev(q, k, v)
     out, lse = dit_attn.attention(qd, kd, vd, 2, with_lse=False)
     assert lse is None
-    check_attention(out, None, o_ref, None, "no lse")
+    check_attention(out, None, o_ref, None, f"no lse D={D}")
+    # the LSE output changes nothing else
+    out2, _ = dit_attn.attention(qd, kd, vd, 2)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2)
 
 
 # ------------------------------------------------- partials + standalone merge
@@ -309,11 +314,11 @@ def test_partials_then_merge(name, n):
     check_f32(out, m_ref, f"{name} merge of gpu partials")
 
 
-def test_repeatable_bitwise():
-    cfg = workloads.BY_NAME["tiny"]
-    q, k, v = to_dev(*workloads.make_qkv(cfg))
-    a, la = dit_attn.attention(q, k, v, 2)
-    b, lb = dit_attn.attention(q, k, v, 2)
+@pytest.mark.parametrize("D", [64, 72, 128])
+def test_repeatable_bitwise(D):
+    q, k, v = to_dev(*workloads.make_random_qkv(1, 3, 700, D, seed=21))
+    a, la = dit_attn.attention(q, k, v, 3)
+    b, lb = dit_attn.attention(q, k, v, 3)
     assert torch.equal(a, b) and torch.equal(la, lb)
 
 
