@@ -51,8 +51,15 @@
 // made at a chunk boundary, and the largest weight of a row stays exactly 1
 // when it sets the reference.  When m moves, the accumulator and the open
 // chunk's l_c are rescaled together; L is absolute and never rescaled.
-// Key tiles never straddle chunks: a tile that would is cut at the chunk end
-// (columns past it are masked to -inf) and the next chunk starts a new tile.
+// Two key walks.  Chunk by chunk (the default): key tiles never straddle
+// chunks; a tile that would is cut at the chunk end (columns past it are
+// masked to -inf) and the next chunk starts a new tile.  Grid walk (kGrid,
+// every chunk at least one tile long): the tiles lie on the global 128-key
+// grid and a tile that straddles a chunk end is computed once; its PV is
+// shared (same reference, same accumulator) and only its row sum is split at
+// the chunk end: the smaller side is summed again with the same instructions,
+// the other side is the rest.  With chunks of at least one tile, a tile holds
+// at most one chunk end.
 //
 // Epilogue of the merged result: each thread scales its O row by 2^(m - L)
 // and rounds it to bf16.  At D = 72 a warp stages its 32 rows in shared
@@ -160,17 +167,21 @@ struct KvIter {
   }
   __device__ __forceinline__ int valid() const { return min(kBlockN, j1 - t0); }
   __device__ __forceinline__ bool chunk_start() const { return t0 == j0; }
+  // Moves the chunk bounds on to the next chunk.
+  __device__ __forceinline__ void step_chunk(int q, int r, int n) {
+    j0 = j1;
+    j1 += q;
+    rem += r;
+    if (rem >= n) {
+      rem -= n;
+      ++j1;
+    }
+  }
   // q, r, n: the partition (S = q n + r); unused once the last chunk is done.
   __device__ __forceinline__ void next(int q, int r, int n) {
     t0 += kBlockN;
     if (t0 >= j1) {
-      j0 = j1;
-      j1 += q;
-      rem += r;
-      if (rem >= n) {
-        rem -= n;
-        ++j1;
-      }
+      step_chunk(q, r, n);
       t0 = j0;
     }
   }
@@ -289,7 +300,10 @@ __device__ __forceinline__ void store_f32_row(float *dst, const uint32_t *r, int
 //   kernels is a visible share of the time.  Long grids use the plain launch
 //   and a kernel without the two grid-dependency instructions, whose position
 //   in the code measurably cost the D = 64 loop about 2 %.
-template <int D, bool kPartials, bool kPdl>
+// kGrid (merged mode only): the grid walk described at the top.  A separate
+//   instantiation, because its straddle code slows the loop by a few per cent
+//   even where it never runs.
+template <int D, bool kPartials, bool kPdl, bool kGrid = false>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_q_tail,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_k_tail,
@@ -449,7 +463,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tma_load_3d(vd, &tm_v, v_full(s), 0, kv.t0, bh, pol_kv);
         if constexpr (C::kVTail > 0) tma_load_3d(vd + kSwzBytes, &tm_v_tail, v_full(s), 64, kv.t0, bh, pol_kv);
         v_last[s] = u;
-        kv.next(p.chunk_q, p.chunk_r, p.n_chunks);
+        if constexpr (kGrid) kv.t0 += kBlockN;
+        else kv.next(p.chunk_q, p.chunk_r, p.n_chunks);
       }
       // Drain: every load issued must land before the CTA may exit.  Waiting on
       // the parity of a stage's last use returns at once if it already landed.
@@ -605,7 +620,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           tc_fence_before();
           mbar_arrive(s_free(t));
         }
-        const int valid = kv.valid();
+        const int valid = kGrid ? min(kBlockN, p.S - kv.t0) : kv.valid();
         float row_max = hw_max;
         if (valid < kBlockN) {
           // A tile cut at a chunk end or at S: the columns past `valid` are
@@ -627,13 +642,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         const float tmax = row_max * scale_log2;
         float o_scale = 1.0f;
-        if (kv.chunk_start() && it > 0) {
+        if (kGrid ? (kv.j1 == kv.t0 && it > 0) : (kv.chunk_start() && it > 0)) {
           // The previous chunk is complete: fold its LSE into the running one.
           // Its partial output is already in the accumulator with the shared
           // reference m, so the O half of the merge is applied at the end.
           l_run = logaddexp2(l_run, m + lg2_approx(fmaxf(l, 0.0f)));
           l = 0.0f;
+          if constexpr (kGrid) kv.step_chunk(p.chunk_q, p.chunk_r, p.n_chunks);
         }
+        // Grid walk: the open chunk may end strictly inside this tile (at
+        // column b_rel); then the tile's row sum is split there.
+        const int b_rel = kv.j1 - kv.t0;
+        const bool straddle = kGrid && b_rel < valid;
         if (tmax > m + kRescaleThreshold) {
           const float f = ex2_approx(m - tmax);
           o_scale *= f;
@@ -646,6 +666,34 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (it > 0) {
             if (!(ok = mbar_wait_warp(o_upd(t), (it - 1) & 1))) break;
             tc_fence_after();
+          }
+        }
+        // Straddling tile: the sum of P over the smaller side of the chunk end
+        // (at most 64 keys), with the same instructions as the loop below, so
+        // the same values; the other side is the tile's sum minus it.  8-key
+        // groups outside that side are skipped with a warp-uniform branch.
+        float part = 0.0f;
+        bool left_small = true;
+        if constexpr (kGrid) {
+          if (straddle) {
+            left_small = b_rel <= kBlockN / 2;
+            const int lo = left_small ? 0 : b_rel, hi = left_small ? b_rel : valid;
+#pragma unroll
+            for (int g = 0; g < kBlockN / 8; ++g) {
+              if (8 * g + 8 > lo && 8 * g < hi) {
+#pragma unroll
+                for (int i = 0; i < 8; i += 2) {
+                  const int j = 8 * g + i;
+                  float x0, x1;
+                  fma2(x0, x1, __uint_as_float(sr[j]), __uint_as_float(sr[j + 1]), scale_log2, scale_log2, neg_m,
+                       neg_m);
+                  const float a = ex2_approx(x0);
+                  const float b = ex2_approx(x1);
+                  part += (j >= lo && j < hi) ? a : 0.0f;
+                  part += (j + 1 >= lo && j + 1 < hi) ? b : 0.0f;
+                }
+              }
+            }
           }
         }
         // P = 2^(S * scale - m): the affine part on packed pairs, 2^x on the
@@ -669,7 +717,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         add2(acc[0], acc[1], acc[2], acc[3]);
         add2(acc[4], acc[5], acc[6], acc[7]);
         add2(acc[0], acc[1], acc[4], acc[5]);
-        l += acc[0] + acc[1];
+        const float l_tile = acc[0] + acc[1];
+        if (straddle) {
+          // The open chunk ends inside this tile: its LSE takes the keys left
+          // of the end, the next chunk starts with the rest.
+          const float l_left = left_small ? part : fmaxf(l_tile - part, 0.0f);
+          const float l_right = left_small ? fmaxf(l_tile - part, 0.0f) : part;
+          l_run = logaddexp2(l_run, m + lg2_approx(fmaxf(l + l_left, 0.0f)));
+          l = l_right;
+          kv.step_chunk(p.chunk_q, p.chunk_r, p.n_chunks);
+        } else {
+          l += l_tile;
+        }
         // O may be rescaled after P is written: the PV MMA that reads both waits
         // for this warpgroup's arrival below.  Doing it here, once the S values
         // are dead, keeps the row in registers without spilling.
@@ -677,7 +736,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(p_full(t));
-        kv.next(p.chunk_q, p.chunk_r, p.n_chunks);
+        if constexpr (kGrid) kv.t0 += kBlockN;
+        else kv.next(p.chunk_q, p.chunk_r, p.n_chunks);
       }
       if (ok) ok = mbar_wait_warp(o_full(t), 0);
       if (ok) {

@@ -266,6 +266,27 @@ def test_attention_chunks_shorter_than_a_tile(D):
     check_attention(merged.to(torch.bfloat16), mlse, o_ref, l_ref, f"D={D} n=S partials+merge", abs_ref=a_ref)
 
 
+# D = 128 with every chunk at least one tile long and chunk ends inside tiles:
+# the merged launch takes the grid walk (a straddling tile computed once, its
+# row sum split at the chunk end).  Ends inside tiles only (1000/3, 1152/2),
+# inside and on tile boundaries (1344/3: 448, 896), almost every tile
+# straddling (2000/15: 133-134 keys), a ragged last tile throughout but 1152.
+@pytest.mark.parametrize("S,n", [(1000, 3), (1152, 2), (1344, 3), (2000, 15)])
+def test_attention_grid_walk_d128(S, n):
+    q, k, v = workloads.make_random_qkv(2, 2, S, 128, seed=S + n)
+    qf, kf, vf = f64(q), f64(k), f64(v)
+    o_ref, l_ref = oracle.attention(qf, kf, vf)
+    out, lse = run_attention(q, k, v, n)
+    check_attention(out, lse, o_ref, l_ref, f"grid walk S={S} n={n}")
+    # the same chunks as partials, merged afterwards
+    parts, lses = dit_attn.attention_partials(*to_dev(q, k, v), n)
+    merged, mlse = dit_attn.merge(parts, lses)
+    torch.cuda.synchronize()
+    assert_no_device_error()
+    assert (out.float().cpu() - merged.reshape(out.shape).cpu()).abs().max().item() <= 2e-2
+    assert (lse.cpu() - mlse.reshape(lse.shape).cpu()).abs().max().item() <= 1e-3
+
+
 @pytest.mark.parametrize("D", [64, 72, 128])
 def test_attention_sharp_softmax(D):
     # large logits: the reference max moves often and by a lot, so O is
